@@ -1,0 +1,254 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention (fwd + bwd).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import
+this package.  The product library never imports it and shares no code with
+it; the two meet only in the seeded input generators of ``fa_inputs``.
+
+The arithmetic lives in ``fa_oracle.c`` (plain C, IEEE double, libm exp/log).
+This module compiles it with gcc on first use and marshals numpy arrays.
+
+What each function follows:
+
+* ``forward``: the attention definition in "What is Flash Attention?"
+  (transcript 01:04: S = QK^T/sqrt(d), row softmax, O = PV) with the safe
+  softmax of "Atencao exata, acelerada por nunca escrever a grade gigante."
+  (softmax formula with m = max_j x_j); the stored statistic is
+  lse = m + ln l, the pair (m, l) kept per row (transcript 06:52).
+* ``backward``: the plain chain rule through that definition (the pages state
+  only that gradients are exact and that P is recomputed, transcript
+  06:52-07:24 and 08:26).
+* ``online_softmax`` / ``online_attention_row``: the running-max update of
+  transcript 04:46-05:17, used only to pin online == two-pass.
+
+Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "fa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libfa_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_library(src: str, out: str) -> str:
+    """Compile a copy of the oracle's C source into a shared library."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-add, so every product and sum is a
+    # separately rounded IEEE double operation, identical on x86 and Arm.
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-fno-fast-math", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into oracle/_build/libfa_oracle.so (gcc, -O2)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE)):
+        return _LIB_PATH
+    return compile_library(SOURCE, _LIB_PATH)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(x) -> np.ndarray:
+    """Exact conversion to a C-contiguous float64 array (bf16 -> f64 is exact)."""
+    if hasattr(x, "detach"):  # a torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _iptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _sel(rows, BH: int, N: int):
+    if rows is None:
+        return None, BH * N
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    if r.size and (r.min() < 0 or r.max() >= BH * N):
+        raise ValueError("row index out of range")
+    return r, int(r.size)
+
+
+def _shape(q):
+    if q.ndim == 4:
+        B, H, N, d = q.shape
+        return B * H, N, d
+    if q.ndim == 3:
+        BH, N, d = q.shape
+        return BH, N, d
+    raise ValueError("expected [B,H,N,d] or [BH,N,d]")
+
+
+class Oracle:
+    """The oracle bound to one compiled copy of fa_oracle.c."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int64)
+        i, d, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+        lib.fa_oracle_forward.argtypes = [dp, dp, dp, i, i, i, d, i, ip, i64, dp, dp, i]
+        lib.fa_oracle_backward_rows.argtypes = [dp, dp, dp, dp, i, i, i, d, i, ip, i64,
+                                                dp, dp, dp, dp, dp, i]
+        lib.fa_oracle_backward_cols.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, d, i,
+                                                ip, i64, dp, dp, i]
+        lib.fa_oracle_online_softmax.argtypes = [dp, i, i, dp, dp]
+        lib.fa_oracle_online_attention_row.argtypes = [dp, dp, i, i, i, dp, dp]
+        for f in (lib.fa_oracle_forward, lib.fa_oracle_backward_rows,
+                  lib.fa_oracle_backward_cols, lib.fa_oracle_online_softmax,
+                  lib.fa_oracle_online_attention_row):
+            f.restype = ctypes.c_int
+        self.lib = lib
+        self.path = lib_path
+
+    def forward(self, q, k, v, scale: float, causal: bool, rows=None,
+                nthreads: int | None = None):
+        """O and lse of the definition.
+
+        q, k, v: [B,H,N,d] or [BH,N,d] (any dtype; converted exactly to float64).
+        rows: None for every row, else flat indices bh*N + i.
+        Returns (o, lse): o is [BH*N, d] (or [len(rows), d]), lse [BH*N] (or [len(rows)]).
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        BH, N, d = _shape(q)
+        sel, n = _sel(rows, BH, N)
+        o = np.empty((n, d), np.float64)
+        lse = np.empty((n,), np.float64)
+        rc = self.lib.fa_oracle_forward(
+            _ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n,
+            _ptr(o), _ptr(lse), int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"fa_oracle_forward failed ({rc})")
+        return o, lse
+
+    def backward_rows(self, q, k, v, dO, scale: float, causal: bool, rows=None,
+                      nthreads: int | None = None):
+        """Row pass: dq for the selected rows plus per-row m, l, D and D_alt.
+
+        D is sum_j P_ij dP_ij; D_alt is sum_c dO_ic O_ic.  They agree exactly in
+        real arithmetic; the pins check they agree to fp64 rounding.
+        """
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        BH, N, d = _shape(q)
+        sel, n = _sel(rows, BH, N)
+        dq = np.empty((n, d), np.float64)
+        m = np.empty((n,), np.float64)
+        l = np.empty((n,), np.float64)
+        D = np.empty((n,), np.float64)
+        D_alt = np.empty((n,), np.float64)
+        rc = self.lib.fa_oracle_backward_rows(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dO), BH, N, d, float(scale), int(bool(causal)),
+            _iptr(sel), n, _ptr(dq), _ptr(m), _ptr(l), _ptr(D), _ptr(D_alt),
+            int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"fa_oracle_backward_rows failed ({rc})")
+        return dq, m, l, D, D_alt
+
+    def backward_cols(self, q, k, v, dO, m_all, l_all, D_all, scale: float, causal: bool,
+                      cols=None, nthreads: int | None = None):
+        """Column pass: dk, dv for the selected key rows (flat bh*N + j).
+
+        m_all, l_all, D_all must cover every row (from backward_rows(rows=None)).
+        """
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        m_all, l_all, D_all = _f64(m_all), _f64(l_all), _f64(D_all)
+        BH, N, d = _shape(q)
+        if m_all.size != BH * N or l_all.size != BH * N or D_all.size != BH * N:
+            raise ValueError("m_all, l_all, D_all must hold every row")
+        sel, n = _sel(cols, BH, N)
+        dk = np.empty((n, d), np.float64)
+        dv = np.empty((n, d), np.float64)
+        rc = self.lib.fa_oracle_backward_cols(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(m_all), _ptr(l_all), _ptr(D_all),
+            BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n, _ptr(dk), _ptr(dv),
+            int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"fa_oracle_backward_cols failed ({rc})")
+        return dk, dv
+
+    def backward(self, q, k, v, dO, scale: float, causal: bool, nthreads: int | None = None):
+        """Full backward: (dq, dk, dv) each [BH*N, d], plus (m, l, D, D_alt) per row."""
+        dq, m, l, D, D_alt = self.backward_rows(q, k, v, dO, scale, causal, None, nthreads)
+        dk, dv = self.backward_cols(q, k, v, dO, m, l, D, scale, causal, None, nthreads)
+        return dq, dk, dv, (m, l, D, D_alt)
+
+    def online_softmax(self, x, block: int):
+        """Running (m, l) after each block of the row x (online update)."""
+        x = _f64(x).reshape(-1)
+        nb = -(-x.size // block)
+        m = np.empty((nb,), np.float64)
+        l = np.empty((nb,), np.float64)
+        rc = self.lib.fa_oracle_online_softmax(_ptr(x), x.size, int(block), _ptr(m), _ptr(l))
+        if rc != nb:
+            raise RuntimeError(f"fa_oracle_online_softmax failed ({rc})")
+        return m, l
+
+    def online_attention_row(self, s, v, block: int):
+        """One attention row by the online update: (o [d], lse)."""
+        s = _f64(s).reshape(-1)
+        v = _f64(v)
+        n, d = v.shape
+        if s.size != n:
+            raise ValueError("s and v disagree on n")
+        o = np.empty((d,), np.float64)
+        lse = np.empty((1,), np.float64)
+        rc = self.lib.fa_oracle_online_attention_row(_ptr(s), _ptr(v), n, d, int(block),
+                                                     _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise RuntimeError(f"fa_oracle_online_attention_row failed ({rc})")
+        return o, float(lse[0])
+
+
+def default() -> Oracle:
+    """The oracle compiled from oracle/fa_oracle.c (built on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def forward(*a, **kw):
+    return default().forward(*a, **kw)
+
+
+def backward_rows(*a, **kw):
+    return default().backward_rows(*a, **kw)
+
+
+def backward_cols(*a, **kw):
+    return default().backward_cols(*a, **kw)
+
+
+def backward(*a, **kw):
+    return default().backward(*a, **kw)
+
+
+def online_softmax(*a, **kw):
+    return default().online_softmax(*a, **kw)
+
+
+def online_attention_row(*a, **kw):
+    return default().online_attention_row(*a, **kw)

@@ -1,0 +1,360 @@
+/*
+ * fa_oracle.c — plain, slow, fp64 CPU oracle for exact scaled-dot-product
+ * attention and its gradients.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file.  Only the tests, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py use it.  It shares no code,
+ * header, table or constant with the CUDA path.
+ *
+ * Sources followed (web pages on FlashAttention):
+ *  - "What is Flash Attention?" (Data Science in your pocket), transcript
+ *    01:04: S = Q K^T / sqrt(d), softmax row by row to P, O = P V.
+ *  - "Atencao exata, acelerada por nunca escrever a grade gigante."
+ *    (mentria.ai), safe-softmax formula: softmax(x)_i = e^{x_i-m} / sum_j
+ *    e^{x_j-m} with m = max_j x_j; and o_flash = o_exact (the tiled method
+ *    reaches the plain definition exactly, so the oracle IS the definition).
+ *  - "What is Flash Attention?", transcript 04:46-05:17: the online-softmax
+ *    update (m' = max(m, m_blk), alpha = e^{m-m'}, beta = e^{m_blk-m'},
+ *    l' = alpha l + beta sum e^{x-m_blk}, O_acc <- alpha O_acc + beta P_blk
+ *    V_blk, divide by l at the end).  Used here ONLY by the pin helpers
+ *    (online == two-pass), never by the definition functions.
+ *  - "What is Flash Attention?", transcript 06:52-07:24: only O and two
+ *    per-row statistics (m, l) are kept; P is rebuilt in the backward pass.
+ *    The gradient formulas are not printed on the pages; they are the plain
+ *    chain rule of L(O) through the definition above:
+ *      dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij,
+ *      dS_ij = P_ij (dP_ij - D_i),  dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ * Readings where the pages are silent:
+ *  - causal: key j is visible to query i iff j <= i (square, top-left
+ *    aligned); masked scores are -inf before the softmax.
+ *  - the stored statistic is lse_i = m_i + ln l_i (natural log of the scaled
+ *    scores), which is the pair (m, l) folded into one number.
+ *
+ * Layout: every [BH][N][d] array is row-major with index (bh*N + i)*d + c.
+ * Row / column selections are flat indices r = bh*N + i.
+ * All arithmetic is IEEE double; libm exp/log only.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* a minimal work-sharing loop over items (no arithmetic of the method) */
+
+typedef void (*item_fn)(void* ctx, int64_t item, double* scratch);
+
+typedef struct {
+  item_fn fn;
+  void* ctx;
+  int64_t n_items;
+  int64_t next; /* shared counter */
+  size_t scratch_doubles;
+  int failed;
+} pool_t;
+
+static void* pool_worker(void* arg) {
+  pool_t* p = (pool_t*)arg;
+  double* scratch = (double*)malloc(sizeof(double) * (p->scratch_doubles + 1));
+  if (!scratch) {
+    __atomic_store_n(&p->failed, 1, __ATOMIC_SEQ_CST);
+    return NULL;
+  }
+  for (;;) {
+    int64_t it = __atomic_fetch_add(&p->next, 1, __ATOMIC_SEQ_CST);
+    if (it >= p->n_items) break;
+    p->fn(p->ctx, it, scratch);
+  }
+  free(scratch);
+  return NULL;
+}
+
+static int run_pool(item_fn fn, void* ctx, int64_t n_items, size_t scratch_doubles,
+                    int nthreads) {
+  pool_t p;
+  p.fn = fn;
+  p.ctx = ctx;
+  p.n_items = n_items;
+  p.next = 0;
+  p.scratch_doubles = scratch_doubles;
+  p.failed = 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 512) nthreads = 512;
+  if ((int64_t)nthreads > n_items) nthreads = (int)(n_items > 0 ? n_items : 1);
+  if (nthreads == 1) {
+    pool_worker(&p);
+    return p.failed ? -1 : 0;
+  }
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return -1;
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, pool_worker, &p) != 0) break;
+    ++started;
+  }
+  if (started == 0) pool_worker(&p);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  free(th);
+  return p.failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* the definition                                                       */
+
+typedef struct {
+  const double *q, *k, *v, *dO;
+  int BH, N, d, causal;
+  double scale;
+  const int64_t* sel; /* selected flat rows / columns, or NULL = all */
+  /* forward outputs */
+  double *o, *lse;
+  /* backward-row outputs */
+  double *dq, *m_out, *l_out, *D_out, *D_alt_out;
+  /* backward-column inputs/outputs */
+  const double *m_all, *l_all, *D_all;
+  double *dk, *dv;
+} job_t;
+
+/* s_ij = scale * sum_c q_ic k_jc, or -inf when causal and j > i. */
+static double score(const job_t* J, int64_t bh, int i, int j) {
+  if (J->causal && j > i) return -INFINITY;
+  const double* qi = J->q + ((size_t)bh * J->N + i) * J->d;
+  const double* kj = J->k + ((size_t)bh * J->N + j) * J->d;
+  double acc = 0.0;
+  for (int c = 0; c < J->d; ++c) acc += qi[c] * kj[c];
+  return J->scale * acc;
+}
+
+/* Row i of S and P written out in full (scratch holds 2N doubles):
+ * s_j, m = max_j s_j, l = sum_j e^{s_j - m}, p_j = e^{s_j - m} / l. */
+static void softmax_row(const job_t* J, int64_t bh, int i, double* s, double* p,
+                        double* m_ret, double* l_ret) {
+  const int N = J->N;
+  double m = -INFINITY;
+  for (int j = 0; j < N; ++j) {
+    s[j] = score(J, bh, i, j);
+    if (s[j] > m) m = s[j];
+  }
+  double l = 0.0;
+  for (int j = 0; j < N; ++j) l += exp(s[j] - m); /* e^{-inf} = 0 */
+  for (int j = 0; j < N; ++j) p[j] = exp(s[j] - m) / l;
+  *m_ret = m;
+  *l_ret = l;
+}
+
+static void fwd_item(void* ctx, int64_t it, double* scratch) {
+  const job_t* J = (const job_t*)ctx;
+  const int64_t r = J->sel ? J->sel[it] : it;
+  const int64_t bh = r / J->N;
+  const int i = (int)(r % J->N);
+  double* s = scratch;
+  double* p = scratch + J->N;
+  double m, l;
+  softmax_row(J, bh, i, s, p, &m, &l);
+  double* oi = J->o + (size_t)it * J->d;
+  for (int c = 0; c < J->d; ++c) {
+    double acc = 0.0;
+    for (int j = 0; j < J->N; ++j)
+      acc += p[j] * J->v[((size_t)bh * J->N + j) * J->d + c];
+    oi[c] = acc;
+  }
+  J->lse[it] = m + log(l);
+}
+
+/* O = P V and lse = m + ln l for the selected rows (all rows when sel is
+ * NULL).  o is [n_rows][d], lse is [n_rows]. */
+int fa_oracle_forward(const double* q, const double* k, const double* v, int BH, int N, int d,
+                      double scale, int causal, const int64_t* sel, int64_t n_rows, double* o,
+                      double* lse, int nthreads) {
+  if (!q || !k || !v || !o || !lse || BH < 1 || N < 1 || d < 1) return -1;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.q = q; J.k = k; J.v = v;
+  J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
+  J.sel = sel; J.o = o; J.lse = lse;
+  if (!sel) n_rows = (int64_t)BH * N;
+  return run_pool(fwd_item, &J, n_rows, (size_t)2 * N, nthreads);
+}
+
+static void bwd_row_item(void* ctx, int64_t it, double* scratch) {
+  const job_t* J = (const job_t*)ctx;
+  const int64_t r = J->sel ? J->sel[it] : it;
+  const int64_t bh = r / J->N;
+  const int i = (int)(r % J->N);
+  const int N = J->N, d = J->d;
+  double* s = scratch;
+  double* p = scratch + N;
+  double* dP = scratch + 2 * (size_t)N;
+  double m, l;
+  softmax_row(J, bh, i, s, p, &m, &l);
+  const double* dOi = J->dO + ((size_t)bh * N + i) * d;
+  /* dP_ij = sum_c dO_ic v_jc */
+  for (int j = 0; j < N; ++j) {
+    const double* vj = J->v + ((size_t)bh * N + j) * d;
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += dOi[c] * vj[c];
+    dP[j] = acc;
+  }
+  /* D_i from its definition sum_j P_ij dP_ij ... */
+  double D = 0.0;
+  for (int j = 0; j < N; ++j) D += p[j] * dP[j];
+  /* ... and from sum_c dO_ic o_ic with o_i = sum_j p_ij v_j */
+  double D_alt = 0.0;
+  for (int c = 0; c < d; ++c) {
+    double oc = 0.0;
+    for (int j = 0; j < N; ++j) oc += p[j] * J->v[((size_t)bh * N + j) * d + c];
+    D_alt += dOi[c] * oc;
+  }
+  /* dQ_i = scale * sum_j dS_ij k_j with dS_ij = p_ij (dP_ij - D_i) */
+  double* dqi = J->dq + (size_t)it * d;
+  for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+  for (int j = 0; j < N; ++j) {
+    const double dS = p[j] * (dP[j] - D);
+    const double* kj = J->k + ((size_t)bh * N + j) * d;
+    for (int c = 0; c < d; ++c) dqi[c] += dS * kj[c];
+  }
+  for (int c = 0; c < d; ++c) dqi[c] *= J->scale;
+  if (J->m_out) J->m_out[it] = m;
+  if (J->l_out) J->l_out[it] = l;
+  if (J->D_out) J->D_out[it] = D;
+  if (J->D_alt_out) J->D_alt_out[it] = D_alt;
+}
+
+/* Row pass of the backward for the selected rows: dq [n][d], and the
+ * per-row m, l, D (both forms of D, which must agree).  Any of m_out,
+ * l_out, D_out, D_alt_out may be NULL. */
+int fa_oracle_backward_rows(const double* q, const double* k, const double* v, const double* dO,
+                            int BH, int N, int d, double scale, int causal, const int64_t* sel,
+                            int64_t n_rows, double* dq, double* m_out, double* l_out,
+                            double* D_out, double* D_alt_out, int nthreads) {
+  if (!q || !k || !v || !dO || !dq || BH < 1 || N < 1 || d < 1) return -1;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.q = q; J.k = k; J.v = v; J.dO = dO;
+  J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
+  J.sel = sel; J.dq = dq; J.m_out = m_out; J.l_out = l_out;
+  J.D_out = D_out; J.D_alt_out = D_alt_out;
+  if (!sel) n_rows = (int64_t)BH * N;
+  return run_pool(bwd_row_item, &J, n_rows, (size_t)3 * N, nthreads);
+}
+
+static void bwd_col_item(void* ctx, int64_t it, double* scratch) {
+  (void)scratch;
+  const job_t* J = (const job_t*)ctx;
+  const int64_t r = J->sel ? J->sel[it] : it;
+  const int64_t bh = r / J->N;
+  const int j = (int)(r % J->N);
+  const int N = J->N, d = J->d;
+  const double* vj = J->v + ((size_t)bh * N + j) * d;
+  double* dkj = J->dk + (size_t)it * d;
+  double* dvj = J->dv + (size_t)it * d;
+  for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+  for (int i = 0; i < N; ++i) {
+    const double s = score(J, bh, i, j);
+    if (s == -INFINITY) continue; /* p_ij = 0 exactly */
+    const int64_t ri = bh * N + i;
+    const double p = exp(s - J->m_all[ri]) / J->l_all[ri];
+    const double* dOi = J->dO + (size_t)ri * d;
+    const double* qi = J->q + (size_t)ri * d;
+    double dP = 0.0;
+    for (int c = 0; c < d; ++c) dP += dOi[c] * vj[c];
+    const double dS = p * (dP - J->D_all[ri]);
+    for (int c = 0; c < d; ++c) {
+      dvj[c] += p * dOi[c];  /* dV = P^T dO */
+      dkj[c] += dS * qi[c];  /* dK = scale dS^T Q */
+    }
+  }
+  for (int c = 0; c < d; ++c) dkj[c] *= J->scale;
+}
+
+/* Column pass of the backward for the selected key rows j: dk, dv [n][d].
+ * Needs m, l, D of EVERY row ([BH*N] each, from fa_oracle_backward_rows with
+ * sel = NULL), since column j of P touches all rows. */
+int fa_oracle_backward_cols(const double* q, const double* k, const double* v, const double* dO,
+                            const double* m_all, const double* l_all, const double* D_all,
+                            int BH, int N, int d, double scale, int causal, const int64_t* sel,
+                            int64_t n_cols, double* dk, double* dv, int nthreads) {
+  if (!q || !k || !v || !dO || !m_all || !l_all || !D_all || !dk || !dv || BH < 1 || N < 1 ||
+      d < 1)
+    return -1;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.q = q; J.k = k; J.v = v; J.dO = dO;
+  J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
+  J.sel = sel; J.m_all = m_all; J.l_all = l_all; J.D_all = D_all;
+  J.dk = dk; J.dv = dv;
+  if (!sel) n_cols = (int64_t)BH * N;
+  return run_pool(bwd_col_item, &J, n_cols, 1, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* online-softmax helpers, used only to pin the online update against
+ * the two-pass definition ("What is Flash Attention?", 04:46-05:17).    */
+
+/* Row x[0..n) processed in blocks of `block` entries.  After block b the
+ * running (m, l) are written to m_trace[b], l_trace[b].  Returns the number
+ * of blocks.  The block sum is taken relative to the block max m_blk and
+ * put on the running scale with beta = e^{m_blk - m'}. */
+int fa_oracle_online_softmax(const double* x, int n, int block, double* m_trace,
+                             double* l_trace) {
+  if (!x || n < 1 || block < 1) return -1;
+  double m = -INFINITY, l = 0.0;
+  int nb = 0;
+  for (int start = 0; start < n; start += block, ++nb) {
+    const int end = start + block < n ? start + block : n;
+    double m_blk = -INFINITY;
+    for (int t = start; t < end; ++t)
+      if (x[t] > m_blk) m_blk = x[t];
+    double m_new = m > m_blk ? m : m_blk;
+    double alpha, beta, blk_sum = 0.0;
+    if (m_new == -INFINITY) { /* every entry so far is -inf */
+      alpha = 0.0; beta = 0.0;
+    } else {
+      alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+      beta = (m_blk == -INFINITY) ? 0.0 : exp(m_blk - m_new);
+      if (m_blk != -INFINITY)
+        for (int t = start; t < end; ++t) blk_sum += exp(x[t] - m_blk);
+    }
+    l = alpha * l + beta * blk_sum;
+    m = m_new;
+    if (m_trace) m_trace[nb] = m;
+    if (l_trace) l_trace[nb] = l;
+  }
+  return nb;
+}
+
+/* One attention row done the online way: scores s[0..n), values v [n][d],
+ * blocks of `block` keys.  O_acc <- alpha O_acc + beta P_blk V_blk with
+ * P_blk = e^{s - m_blk}; at the end o = O_acc / l and lse = m + ln l. */
+int fa_oracle_online_attention_row(const double* s, const double* v, int n, int d, int block,
+                                   double* o, double* lse) {
+  if (!s || !v || !o || !lse || n < 1 || d < 1 || block < 1) return -1;
+  double m = -INFINITY, l = 0.0;
+  for (int c = 0; c < d; ++c) o[c] = 0.0;
+  for (int start = 0; start < n; start += block) {
+    const int end = start + block < n ? start + block : n;
+    double m_blk = -INFINITY;
+    for (int t = start; t < end; ++t)
+      if (s[t] > m_blk) m_blk = s[t];
+    if (m_blk == -INFINITY) continue; /* a fully masked block adds nothing */
+    const double m_new = m > m_blk ? m : m_blk;
+    const double alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+    const double beta = exp(m_blk - m_new);
+    double blk_sum = 0.0;
+    for (int c = 0; c < d; ++c) o[c] *= alpha;
+    for (int t = start; t < end; ++t) {
+      const double pt = exp(s[t] - m_blk);
+      blk_sum += pt;
+      for (int c = 0; c < d; ++c) o[c] += beta * pt * v[(size_t)t * d + c];
+    }
+    l = alpha * l + beta * blk_sum;
+    m = m_new;
+  }
+  if (!(l > 0.0)) return -2; /* every score was -inf: undefined row */
+  for (int c = 0; c < d; ++c) o[c] /= l;
+  *lse = m + log(l);
+  return 0;
+}

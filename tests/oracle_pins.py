@@ -1,0 +1,335 @@
+"""Pins of the fp64 oracle to facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with something other than itself: a worked example printed on
+a page, a closed form, an invariant of the definition, brute force on tiny
+rows, finite differences, or an independent library routine.  The test module
+runs them on the real oracle; the mutant test compiles the oracle with planted
+mistakes and checks that every mistake fails at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, val = line.partition("=")
+            parts = val.split()
+            vals[key.strip()] = [float(p) for p in parts] if len(parts) > 1 else float(parts[0])
+    return vals
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = np.abs(a - b)
+    bound = atol + rtol * np.abs(b)
+    if not np.all(err <= bound):
+        i = int(np.argmax(err - bound))
+        raise AssertionError(f"{what}: max excess at {i}: {a.reshape(-1)[i]!r} vs "
+                             f"{b.reshape(-1)[i]!r} (err {err.reshape(-1)[i]:.3e})")
+
+
+# ---------------------------------------------------------------- pin 1
+def pin_worked_example(orc):
+    """The page's worked online-softmax example (scores 1 2 3 0, blocks of two),
+    "What is Flash Attention?" transcript 05:49-06:52, within the page's
+    rounding; and the same numbers to 1e-12 against their closed forms."""
+    g = _read_golden("online_softmax_worked_example.txt")
+    x = np.array(g["scores"])
+    m, l = orc.online_softmax(x, int(g["block"]))
+    tol = g["page_tolerance"]
+    assert m[0] == g["m1"] and m[1] == g["m2"], (m, g)
+    _close(l[0], g["l1"], tol, what="l1 vs page")
+    _close(l[1], g["l2"], tol, what="l2 vs page")
+    alpha = math.exp(m[0] - m[1])
+    _close(alpha, g["alpha"], tol, what="alpha vs page")
+    _close(alpha * l[0], g["alpha_l1"], tol, what="alpha*l1 vs page")
+    _close(l[1] - alpha * l[0], g["block2_sum"], tol, what="block-2 sum vs page")
+    _close(l[1] / math.exp(-m[1]), g["denominator"], tol, what="denominator vs page")
+    # closed forms
+    _close(l[0], math.exp(-1.0) + 1.0, 1e-12, what="l1 closed form")
+    denom = math.exp(1) + math.exp(2) + math.exp(3) + math.exp(0)
+    _close(l[1], math.exp(-3.0) * denom, 1e-12, what="l2 closed form")
+    # the same row through the definition: q = e_0, k_j = (s_j, 0, ...), v = I.
+    q = np.zeros((1, 1, 4))
+    q[0, 0, 0] = 1.0
+    k = np.zeros((1, 4, 4))
+    k[0, :, 0] = x
+    v = np.eye(4).reshape(1, 4, 4)
+    qq = np.repeat(q, 4, axis=1)  # every query row equal
+    o, lse = orc.forward(qq, k, v, 1.0, False)
+    p_exact = np.exp(x) / denom
+    _close(o[0], p_exact, 1e-12, atol=1e-15, what="softmax of the worked row")
+    _close(lse[0], math.log(denom), 1e-12, what="lse of the worked row")
+    _close(lse[0], m[1] + math.log(l[1]), 1e-12, what="lse == m + ln l")
+
+
+# ---------------------------------------------------------------- pin 2
+def pin_zero_query(orc):
+    """Q = 0 makes every visible score 0: O is the mean of the visible V rows
+    and lse = ln(#visible)."""
+    rng = _rng(2)
+    BH, N, d = 3, 37, 8
+    q = np.zeros((BH, N, d))
+    k = rng.standard_normal((BH, N, d))
+    v = rng.standard_normal((BH, N, d))
+    o, lse = orc.forward(q, k, v, 0.3, False)
+    _close(o.reshape(BH, N, d), np.broadcast_to(v.mean(axis=1, keepdims=True), (BH, N, d)),
+           1e-12, atol=1e-14, what="Q=0 non-causal O")
+    _close(lse, np.full(BH * N, math.log(N)), 1e-13, what="Q=0 non-causal lse")
+    o, lse = orc.forward(q, k, v, 0.3, True)
+    prefix = np.cumsum(v, axis=1) / np.arange(1, N + 1)[None, :, None]
+    _close(o.reshape(BH, N, d), prefix, 1e-12, atol=1e-14, what="Q=0 causal O")
+    _close(lse.reshape(BH, N), np.broadcast_to(np.log(np.arange(1, N + 1)), (BH, N)), 1e-13,
+           atol=1e-15, what="Q=0 causal lse")
+
+
+# ---------------------------------------------------------------- pin 3
+def pin_one_hot(orc):
+    """q_i = c e_1, k_{j*} = e_1, other keys orthogonal to e_1, c*scale = 40:
+    O_i = v_{j*} up to N e^{-40} max|v|."""
+    rng = _rng(3)
+    N, d, scale = 50, 8, 0.5
+    c = 40.0 / scale
+    k = rng.standard_normal((1, N, d))
+    k[0, :, 0] = 0.0
+    q = rng.standard_normal((1, N, d))
+    q[0, :, :] = 0.0
+    q[0, :, 0] = c
+    js = rng.integers(0, N)
+    k[0, js, :] = 0.0
+    k[0, js, 0] = 1.0
+    v = rng.standard_normal((1, N, d))
+    o, lse = orc.forward(q, k, v, scale, False)
+    bound = N * math.exp(-40.0) * np.abs(v).max() * 2
+    _close(o, np.broadcast_to(v[0, js], (N, d)), 0.0, atol=bound, what="one-hot O")
+    _close(lse, np.full(N, 40.0), 0.0, atol=N * math.exp(-40.0) * 2, what="one-hot lse")
+    # causal: for rows i >= j* the key j* dominates; for rows i < j*, scores are
+    # all 0 (keys orthogonal to e_1) so O_i is the prefix mean
+    o, lse = orc.forward(q, k, v, scale, True)
+    o = o.reshape(N, d)
+    for i in range(N):
+        if i >= js:
+            _close(o[i], v[0, js], 0.0, atol=bound, what=f"causal one-hot row {i}")
+        else:
+            _close(o[i], v[0, : i + 1].mean(axis=0), 1e-12, atol=1e-14,
+                   what=f"causal prefix row {i}")
+
+
+# ---------------------------------------------------------------- pin 4
+def pin_permutation(orc):
+    """Jointly permuting the rows of K and V (non-causal) leaves O, lse and dQ
+    unchanged and permutes dK and dV the same way."""
+    rng = _rng(4)
+    BH, N, d, scale = 2, 29, 16, 0.25
+    q, k, v, dO = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    perm = rng.permutation(N)
+    o1, l1 = orc.forward(q, k, v, scale, False)
+    o2, l2 = orc.forward(q, k[:, perm], v[:, perm], scale, False)
+    _close(o2, o1, 1e-12, atol=1e-14, what="perm O")
+    _close(l2, l1, 1e-13, what="perm lse")
+    dq1, dk1, dv1, _ = orc.backward(q, k, v, dO, scale, False)
+    dq2, dk2, dv2, _ = orc.backward(q, k[:, perm], v[:, perm], dO, scale, False)
+    _close(dq2, dq1, 1e-11, atol=1e-13, what="perm dQ")
+    dk1 = dk1.reshape(BH, N, d)[:, perm].reshape(-1, d)
+    dv1 = dv1.reshape(BH, N, d)[:, perm].reshape(-1, d)
+    _close(dk2, dk1, 1e-11, atol=1e-13, what="perm dK")
+    _close(dv2, dv1, 1e-11, atol=1e-13, what="perm dV")
+
+
+# ---------------------------------------------------------------- pin 5
+def _two_pass(x):
+    """Textbook two-pass safe softmax of one row (the brute force)."""
+    m = max(x)
+    if m == -math.inf:
+        return m, 0.0
+    return m, sum(math.exp(t - m) for t in x)
+
+
+def pin_online_equals_two_pass(orc):
+    """Brute force on tiny rows: for n <= 8 and EVERY block size 1..n, the
+    online (m, l) and the online O / lse equal the two-pass values, including
+    rows holding -inf entries."""
+    rng = _rng(5)
+    for n in range(1, 9):
+        for trial in range(3):
+            x = list(rng.standard_normal(n) * 3)
+            if trial == 1 and n > 1:  # some -inf entries, at least one finite
+                for t in rng.choice(n, size=n // 2, replace=False):
+                    x[int(t)] = -math.inf
+            if trial == 2 and n > 2:  # -inf in the leading block
+                x[0] = -math.inf
+            m_ref, l_ref = _two_pass(x)
+            v = rng.standard_normal((n, 3))
+            p_ref = np.array([math.exp(t - m_ref) / l_ref for t in x])
+            o_ref = p_ref @ v
+            for block in range(1, n + 1):
+                m, l = orc.online_softmax(np.array(x), block)
+                assert m[-1] == m_ref, (x, block, m, m_ref)
+                _close(l[-1], l_ref, 1e-13, what=f"online l n={n} block={block}")
+                o, lse = orc.online_attention_row(np.array(x), v, block)
+                _close(o, o_ref, 1e-12, atol=1e-14, what=f"online O n={n} block={block}")
+                _close(lse, m_ref + math.log(l_ref), 1e-13, atol=1e-15,
+                       what=f"online lse n={n} block={block}")
+    # and the online row against the oracle's definition on a real attention row
+    N, d = 8, 4
+    q = rng.standard_normal((1, N, d))
+    k = rng.standard_normal((1, N, d))
+    v = rng.standard_normal((1, N, d))
+    for causal in (False, True):
+        o_def, lse_def = orc.forward(q, k, v, 0.7, causal)
+        for i in range(N):
+            s = 0.7 * (k[0] @ q[0, i])
+            if causal:
+                s[i + 1:] = -math.inf
+            for block in range(1, N + 1):
+                o, lse = orc.online_attention_row(s, v[0], block)
+                _close(o, o_def[i], 1e-12, atol=1e-14, what=f"online vs definition row {i}")
+                _close(lse, lse_def[i], 1e-13, atol=1e-15, what=f"online lse row {i}")
+
+
+# ---------------------------------------------------------------- pin 6
+def pin_finite_differences(orc):
+    """Central differences (h = 1e-6) of L = sum(O * dO) match dQ, dK, dV on
+    B=H=1, N in {1,3,5}, d in {2,4}, causal and not."""
+    rng = _rng(6)
+    h = 1e-6
+    for N in (1, 3, 5):
+        for d in (2, 4):
+            for causal in (False, True):
+                q, k, v, dO = (rng.standard_normal((1, N, d)) for _ in range(4))
+                scale = 1.0 / math.sqrt(d)
+                dq, dk, dv, _ = orc.backward(q, k, v, dO, scale, causal, nthreads=1)
+                grads = {"q": dq, "k": dk, "v": dv}
+
+                def loss(qq, kk, vv):
+                    o, _ = orc.forward(qq, kk, vv, scale, causal, nthreads=1)
+                    return float(np.sum(o.reshape(1, N, d) * dO))
+
+                for name in ("q", "k", "v"):
+                    fd = np.zeros((N, d))
+                    for i in range(N):
+                        for c in range(d):
+                            args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+                            args[name][0, i, c] += h
+                            lp = loss(args["q"], args["k"], args["v"])
+                            args[name][0, i, c] -= 2 * h
+                            lm = loss(args["q"], args["k"], args["v"])
+                            fd[i, c] = (lp - lm) / (2 * h)
+                    g = grads[name].reshape(N, d)
+                    err = np.linalg.norm(fd - g)
+                    assert err <= 1e-7 * max(np.linalg.norm(g), 1e-2), \
+                        (name, N, d, causal, err, np.linalg.norm(g))
+
+
+# ---------------------------------------------------------------- pin 7
+def pin_structure(orc):
+    """Invariants of the definition:
+    * D = sum_j P_ij dP_ij equals sum_c dO_ic O_ic (rows of dS sum to zero);
+    * N = 1: O = V and lse = scale q.k;
+    * O is linear in V;
+    * adding c to every K row leaves O, dQ, dK, dV unchanged and shifts lse_i
+      by scale q_i.c (the row-constant shift cancels in the softmax, and
+      sum_j dS_ij = 0 keeps dQ fixed)."""
+    rng = _rng(7)
+    BH, N, d, scale = 2, 23, 8, 0.35
+    q, k, v, dO = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, m, l, D, D_alt = orc.backward_rows(q, k, v, dO, scale, causal)
+        _close(D, D_alt, 1e-12, atol=1e-13, what="D two ways")
+        o, lse = orc.forward(q, k, v, scale, causal)
+        _close(m + np.log(l), lse, 1e-13, what="m + ln l == lse")
+        _close(D, np.sum(o * dO.reshape(-1, d), axis=1), 1e-11, atol=1e-13,
+               what="D == rowsum(dO*O)")
+    # N = 1
+    q1, k1, v1 = q[:, :1], k[:, :1], v[:, :1]
+    o, lse = orc.forward(q1, k1, v1, scale, False)
+    _close(o, v1.reshape(-1, d), 1e-15, what="N=1 O")
+    _close(lse, scale * np.sum(q1 * k1, axis=2).reshape(-1), 1e-13, atol=1e-15, what="N=1 lse")
+    # linear in V
+    v2 = rng.standard_normal((BH, N, d))
+    for causal in (False, True):
+        oa, _ = orc.forward(q, k, v, scale, causal)
+        ob, _ = orc.forward(q, k, v2, scale, causal)
+        oc, _ = orc.forward(q, k, 2.0 * v - 3.0 * v2, scale, causal)
+        _close(oc, 2.0 * oa - 3.0 * ob, 1e-11, atol=1e-13, what="linear in V")
+    # K shift
+    cvec = rng.standard_normal(d)
+    for causal in (False, True):
+        o1, l1 = orc.forward(q, k, v, scale, causal)
+        o2, l2 = orc.forward(q, k + cvec, v, scale, causal)
+        _close(o2, o1, 1e-10, atol=1e-12, what="K shift O")
+        _close(l2, l1 + scale * (q.reshape(-1, d) @ cvec), 1e-12, atol=1e-13,
+               what="K shift lse")
+        g1 = orc.backward(q, k, v, dO, scale, causal)
+        g2 = orc.backward(q, k + cvec, v, dO, scale, causal)
+        for a, b, nm in zip(g2[:3], g1[:3], ("dQ", "dK", "dV")):
+            _close(a, b, 1e-9, atol=1e-11, what=f"K shift {nm}")
+
+
+# ---------------------------------------------------------------- pin 8
+def pin_torch_sdpa(orc):
+    """Cross-check against an independent implementation: PyTorch's
+    scaled_dot_product_attention in fp64 on the CPU with autograd gradients,
+    and torch.logsumexp for lse."""
+    rng = _rng(8)
+    for (B, H, N, d) in ((2, 3, 37, 16), (1, 2, 130, 8)):
+        for causal in (False, True):
+            q, k, v, dO = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+            scale = 1.0 / math.sqrt(d)
+            tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True)
+                          for a in (q, k, v))
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq, tk, tv, is_causal=causal, scale=scale)
+            to.backward(torch.tensor(dO))
+            s = (tq @ tk.transpose(-1, -2)).detach() * scale
+            if causal:
+                s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), -math.inf)
+            tlse = torch.logsumexp(s, dim=-1).reshape(-1).numpy()
+            o, lse = orc.forward(q, k, v, scale, causal)
+            _close(o, to.detach().reshape(-1, d).numpy(), 1e-10, atol=1e-12, what="sdpa O")
+            _close(lse, tlse, 1e-12, atol=1e-13, what="sdpa lse")
+            dq, dk, dv, _ = orc.backward(q, k, v, dO, scale, causal)
+            for a, t, nm in ((dq, tq, "dQ"), (dk, tk, "dK"), (dv, tv, "dV")):
+                _close(a, t.grad.reshape(-1, d).numpy(), 1e-9, atol=1e-11, what=f"sdpa {nm}")
+
+
+# ---------------------------------------------------------------- pin 9
+def pin_selection_consistency(orc):
+    """Selected-row / selected-column calls return exactly the corresponding
+    rows of the full computation (the sampled checks rely on this)."""
+    rng = _rng(9)
+    BH, N, d, scale = 3, 41, 8, 0.3
+    q, k, v, dO = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    rows = np.array([0, 5, N - 1, N, 2 * N + 7, BH * N - 1])
+    for causal in (False, True):
+        o, lse = orc.forward(q, k, v, scale, causal)
+        os_, ls_ = orc.forward(q, k, v, scale, causal, rows=rows)
+        assert np.array_equal(os_, o[rows]) and np.array_equal(ls_, lse[rows])
+        dq, dk, dv, (m, l, D, _) = orc.backward(q, k, v, dO, scale, causal)
+        dqs, *_ = orc.backward_rows(q, k, v, dO, scale, causal, rows=rows)
+        dks, dvs = orc.backward_cols(q, k, v, dO, m, l, D, scale, causal, cols=rows)
+        assert np.array_equal(dqs, dq[rows])
+        assert np.array_equal(dks, dk[rows]) and np.array_equal(dvs, dv[rows])
+
+
+ALL_PINS = [pin_worked_example, pin_zero_query, pin_one_hot, pin_permutation,
+            pin_online_equals_two_pass, pin_finite_differences, pin_structure,
+            pin_torch_sdpa, pin_selection_consistency]

@@ -1,0 +1,52 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that
+each one fails at least one pin (CPU only).  This shows the pins are strong
+enough to catch a dropped term, a wrong sign, a wrong index or a transposed
+operand anywhere in the oracle."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+# (name, exact text in fa_oracle.c, replacement)
+MUTANTS = [
+    ("dq_scale_dropped", "dqi[c] *= J->scale;", "(void)0;"),
+    ("dk_scale_dropped", "dkj[c] *= J->scale;", "(void)0;"),
+    ("dS_sign", "const double dS = p[j] * (dP[j] - D);", "const double dS = p[j] * (dP[j] + D);"),
+    ("causal_off_by_one", "if (J->causal && j > i) return -INFINITY;",
+     "if (J->causal && j > i + 1) return -INFINITY;"),
+    ("dP_uses_k", "const double* vj = J->v + ((size_t)bh * N + j) * d;\n    double acc = 0.0;",
+     "const double* vj = J->k + ((size_t)bh * N + j) * d;\n    double acc = 0.0;"),
+    ("lse_log2", "J->lse[it] = m + log(l);", "J->lse[it] = m + log2(l);"),
+    ("online_beta_dropped", "l = alpha * l + beta * blk_sum;\n    m = m_new;\n    if (m_trace)",
+     "l = alpha * l + blk_sum;\n    m = m_new;\n    if (m_trace)"),
+    ("dv_uses_dS", "dvj[c] += p * dOi[c];", "dvj[c] += dS * dOi[c];"),
+    ("dk_uses_p", "dkj[c] += dS * qi[c];", "dkj[c] += p * qi[c];"),
+    ("no_max_in_p", "for (int j = 0; j < N; ++j) p[j] = exp(s[j] - m) / l;",
+     "for (int j = 0; j < N; ++j) p[j] = exp(s[j]) / l;"),
+    ("score_transposed", "const double* qi = J->q + ((size_t)bh * J->N + i) * J->d;",
+     "const double* qi = J->q + ((size_t)bh * J->N + j) * J->d;"),
+    ("o_uses_k", "acc += p[j] * J->v[((size_t)bh * J->N + j) * J->d + c];",
+     "acc += p[j] * J->k[((size_t)bh * J->N + j) * J->d + c];"),
+    ("col_pass_D_dropped", "const double dS = p * (dP - J->D_all[ri]);",
+     "const double dS = p * dP;"),
+    ("online_O_alpha_dropped", "for (int c = 0; c < d; ++c) o[c] *= alpha;", "(void)0;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutated = tmp_path / "fa_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, RuntimeError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
