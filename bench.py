@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention fwd+bwd on GB300 through the C ABI of libfa.
+
+One step = one forward pass (fa_forward) and one backward pass (D pre-pass,
+dK/dV kernel, dQ kernel) over one batch of seeded synthetic bf16 inputs
+already resident in device memory.  The default workload is causal attention
+with B=2, H=16, N=8192, d=128, scale 1/sqrt(d) (the long-context case where
+the FLOP target applies).
+
+FLOP convention (algorithmic): forward 4*B*H*N^2*d, backward 10*B*H*N^2*d
+(five matmuls, the S recompute counted once), halved under the causal mask.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle instead (the only other arm this method has), on the host cores.
+Under torchrun every rank runs the same per-GPU workload (weak scaling, no
+collective on the data path; heads are independent).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fa_inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "causal_b2h16n8192d128"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flops(w, causal):
+    base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
+    return 4.0 * base, 10.0 * base
+
+
+def alg_bytes(w):
+    """Algorithmic HBM bytes per step: fwd reads q,k,v and writes o,lse; bwd
+    reads q,k,v,o,dO,lse,D and writes dq,dk,dv (no N^2 terms)."""
+    t = w.B * w.H * w.N * w.d * 2
+    r = w.B * w.H * w.N * 4
+    return 4 * t + r, 8 * t + 2 * r + r  # fwd; bwd incl. D write + read
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def oracle_sample(w, causal, q, k, v, dO, bh_index=0):
+    """Time the fp64 oracle (as it stands) on one (batch, head) pair of the
+    workload: full forward and backward.  Returns (seconds, alg_flops, cores)."""
+    import oracle
+
+    b, h = divmod(bh_index % (w.B * w.H), w.H)
+    qs, ks, vs, ds = (t[b:b + 1, h:h + 1] for t in (q, k, v, dO))
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.forward(qs, ks, vs, w.scale, causal, nthreads=cores)
+    oracle.backward(qs, ks, vs, ds, w.scale, causal, nthreads=cores)
+    dt = time.perf_counter() - t0
+    base = w.N * w.N * w.d * (0.5 if causal else 1.0)
+    return dt, 14.0 * base, cores
+
+
+def run_reference(args, world, rank):
+    w = WORKLOADS[args.workload]
+    causal = w.causal[0]
+    if rank != 0:
+        return 0
+    q, k, v, dO = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    for s in range(args.warmup):
+        oracle_sample(w, causal, q, k, v, dO, s)
+    tot_t, tot_f, cores = 0.0, 0.0, 1
+    for s in range(args.steps):
+        dt, fl, cores = oracle_sample(w, causal, q, k, v, dO, args.warmup + s)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: full fp64 forward+backward of one of the {w.B * w.H} (batch, head) "
+              f"pairs (N={w.N}, d={w.d}, {'causal' if causal else 'full'})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, causal),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, causal):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+            "scale": w.scale, "qk_mult": w.qk_mult, "seed": w.seed,
+            "l2": "inputs larger than L2 (q,k,v,o,dO together "
+                  f"{5 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB per step > 129 MB)"}
+
+
+def run_ours(args, world, rank, local):
+    import exact_io_aware_16_gb300 as fa
+    from exact_io_aware_16_gb300 import build as fabuild
+
+    if rank == 0 or not os.path.exists(fabuild.LIB):
+        fabuild.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    causal = w.causal[0] if args.causal is None else bool(args.causal)
+    scale = w.scale
+    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    D = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
+
+    def step(ev=None):
+        fa.fa_forward(q, k, v, causal=causal, scale=scale, o=o, lse=lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_backward_preprocess(o, dO, D, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, scale=scale, dk=dk, dv=dv,
+                            stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, scale=scale, dq=dq, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {st} {detail:#x}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        evs[s][0].record(stream)
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in timed region: {st} {detail:#x}")
+    total_ms = t_start.elapsed_time(t_end)
+    per_kernel = {n: 0.0 for n in names}
+    for s in range(args.steps):
+        for i, n in enumerate(names):
+            per_kernel[n] += evs[s][i].elapsed_time(evs[s][i + 1])
+    total_ms_max = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms_max / args.steps
+    f_fwd, f_bwd = flops(w, causal)
+    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = read_peaks()
+    long_region = total_ms > 1000.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    peak_kind = "sustained" if long_region else "burst"
+    fwd_ms = per_kernel["fwd"] / args.steps
+    bwd_ms = (per_kernel["bwd_pre"] + per_kernel["bwd_dkdv"] + per_kernel["bwd_dq"]) / args.steps
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+
+    # dominant kernel and its roofline (algorithmic work of that kernel alone)
+    base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
+    kflops = {"fwd": 4 * base, "bwd_dkdv": 8 * base, "bwd_dq": 2 * base, "bwd_pre": 0.0}
+    tbytes = w.B * w.H * w.N * w.d * 2
+    kbytes = {"bwd_pre": 2 * tbytes + w.B * w.H * w.N * 4}
+    dom = max(names, key=lambda n: per_kernel[n])
+    dom_ms = per_kernel[dom] / args.steps
+    if dom == "bwd_pre":
+        ach = kbytes[dom] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None}
+    else:
+        ach = kflops[dom] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "peak_kind": f"{peak_kind} bf16 ({peak_src})"}
+    roof["ms_per_launch"] = dom_ms
+
+    kernels = {}
+    for n in names:
+        ms = per_kernel[n] / args.steps
+        kernels[n] = {"ms_per_launch": ms, "share": per_kernel[n] / max(sum(per_kernel.values()),
+                                                                         1e-9)}
+        if kflops.get(n):
+            kernels[n]["alg_tflops"] = kflops[n] / (ms * 1e-3) / 1e12
+
+    # end to end through the public API, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in (q_h, k_h, v_h, dO_h)]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+        ws = torch.empty(fa.fa_backward_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                         device=dev)
+        dq2, dk2, dv2, o2 = (torch.empty_like(q) for _ in range(4))
+        lse2 = torch.empty_like(lse)
+        qd2, kd2, vd2, dOd2 = (torch.empty_like(q) for _ in range(4))
+
+        def e2e_step():
+            for src, dst in zip(pin, (qd2, kd2, vd2, dOd2)):
+                dst.copy_(src, non_blocking=True)
+            fa.fa_forward(qd2, kd2, vd2, causal=causal, scale=scale, o=o2, lse=lse2, stream=stream)
+            fa.fa_backward(qd2, kd2, vd2, o2, dOd2, lse2, causal=causal, scale=scale, dq=dq2,
+                           dk=dk2, dv=dv2, workspace=ws, stream=stream)
+            for src, dst in zip((o2, lse2, dq2, dk2, dv2), outs_h):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, args.steps // 4)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a0.elapsed_time(a1), world) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": n_e2e}
+        st, detail = fa.fa_get_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error in e2e region: {st} {detail:#x}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, cores = oracle_sample(w, causal, q_h, k_h, v_h, dO_h, 0)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"full fp64 forward+backward of 1 of the {w.B * w.H} (batch, head) "
+                         f"pairs of the workload ({dt:.1f} s; flops counted as 14 N^2 d "
+                         f"{'x 1/2 causal' if causal else ''} for what the oracle computes)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w, causal),
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "fwd_frac_of_peak": fwd_tf / peak, "bwd_frac_of_peak": bwd_tf / peak,
+            "peak_tflops": peak, "peak_source": f"{peak_kind} bf16, {peak_src}",
+            "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--causal", type=int, default=None, help="override the workload's mask mode")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    else:
+        rc = run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,29 @@
+"""Exact IO-aware attention for GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libfa.so`` (declared in
+``include/fa.h``): every step of the attention path runs in the library's CUDA
+kernels; this package only marshals PyTorch tensors into pointers, sizes and a
+stream.  There is no fallback: if the library is missing or the device is not
+sm_103, the calls raise.
+"""
+from ._binding import (  # noqa: F401
+    FaError,
+    fa_backward,
+    fa_backward_dkdv,
+    fa_backward_dq,
+    fa_backward_preprocess,
+    fa_backward_workspace_size,
+    fa_forward,
+    fa_forward_tile_count,
+    fa_get_device_error,
+    fa_status_string,
+    library,
+    library_path,
+)
+
+__all__ = [
+    "FaError", "fa_forward", "fa_backward", "fa_backward_preprocess", "fa_backward_dkdv",
+    "fa_backward_dq",
+    "fa_backward_workspace_size", "fa_forward_tile_count", "fa_get_device_error",
+    "fa_status_string", "library", "library_path",
+]

@@ -1,0 +1,212 @@
+"""ctypes binding of libfa.so: argument marshalling only.
+
+Names and argument order follow ``include/fa.h``.  Tensors must be CUDA bf16
+(inputs/outputs) or fp32 (lse, D) and contiguous; the functions allocate the
+outputs with PyTorch when they are not given.  Calls are asynchronous on the
+current PyTorch stream unless ``stream`` is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(_HERE, "_build", "libfa.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_HEADDIM", -4: "FA_ERR_ALIGN",
+    -5: "FA_ERR_ARCH", -6: "FA_ERR_WORKSPACE", -7: "FA_ERR_CUDA", -8: "FA_ERR_DEVICE_TIMEOUT",
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({fa_status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def library():
+    """Load libfa.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB):
+            raise ImportError(f"libfa.so not built ({_LIB}); run exact_io_aware_16_gb300/build.py")
+        lib = ctypes.CDLL(_LIB)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_forward.restype = i
+        lib.fa_backward_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_backward_workspace_size.restype = sz
+        lib.fa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz,
+                                    vp]
+        lib.fa_backward.restype = i
+        lib.fa_backward_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        lib.fa_backward_preprocess.restype = i
+        lib.fa_backward_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_backward_dkdv.restype = i
+        lib.fa_backward_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_backward_dq.restype = i
+        lib.fa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.fa_get_device_error.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_forward_tile_count.argtypes = [i, i]
+        lib.fa_forward_tile_count.restype = ctypes.c_longlong
+        _lib = lib
+        return lib
+
+
+def fa_status_string(status: int) -> str:
+    return library().fa_status_string(int(status)).decode()
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape=None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def fa_forward_tile_count(N: int, causal: bool) -> int:
+    return int(library().fa_forward_tile_count(int(N), int(bool(causal))))
+
+
+def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+               stream=None):
+    """O = softmax(scale q k^T) v and the per-row lse; q, k, v bf16 [B,H,N,d]."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    st = library().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                              float(scale), int(bool(causal)),
+                              ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward")
+    return o, lse
+
+
+def fa_backward_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(library().fa_backward_workspace_size(B, H, N, d))
+
+
+def fa_backward_preprocess(o, dO, D=None, stream=None):
+    B, H, N, d = o.shape
+    _check(o, "o", torch.bfloat16)
+    _check(dO, "dO", torch.bfloat16, (B, H, N, d))
+    if D is None:
+        D = torch.empty((B, H, N), dtype=torch.float32, device=o.device)
+    _check(D, "D", torch.float32, (B, H, N))
+    st = library().fa_backward_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d,
+                                          ctypes.c_void_p(_stream_handle(stream, o.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_preprocess")
+    return D
+
+
+def fa_backward(q, k, v, o, dO, lse, causal: bool = False, scale: float | None = None,
+                dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """(dq, dk, dv) of the attention; workspace is a uint8 CUDA tensor or None."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    need = fa_backward_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = library().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                               int(bool(causal)), _ptr(workspace), workspace.numel(),
+                               ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward")
+    return dq, dk, dv
+
+
+def fa_backward_dkdv(q, k, v, dO, lse, D, causal: bool = False, scale: float | None = None,
+                     dk=None, dv=None, stream=None):
+    """dk, dv from the D pre-pass output D (fp32 [B,H,N])."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    _check(D, "D", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = library().fa_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
+                                    _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                    int(bool(causal)),
+                                    ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_dkdv")
+    return dk, dv
+
+
+def fa_backward_dq(q, k, v, dO, lse, D, causal: bool = False, scale: float | None = None,
+                   dq=None, stream=None):
+    """dq from the D pre-pass output D (fp32 [B,H,N])."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    _check(D, "D", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    st = library().fa_backward_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
+                                  _ptr(dq), B, H, N, d, float(scale), int(bool(causal)),
+                                  ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_dq")
+    return dq
+
+
+def fa_get_device_error(stream=None):
+    """(status, raw detail word); synchronises the stream."""
+    detail = ctypes.c_uint32(0)
+    dev = torch.cuda.current_device()
+    st = library().fa_get_device_error(ctypes.c_void_p(_stream_handle(stream, dev)),
+                                       ctypes.byref(detail))
+    return st, int(detail.value)

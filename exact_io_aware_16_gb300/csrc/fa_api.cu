@@ -1,0 +1,239 @@
+// fa_api.cu — the C ABI of libfa: argument validation, TMA tensor-map
+// construction and kernel launches.  No device memory is allocated here.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  const long long total = static_cast<long long>(B) * H * N * d;
+  if (total >= (1ll << 31)) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+int check_scale(float scale) {
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+// Is the current device an sm_103 part?  Cached per device ordinal.
+int check_arch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FA_ERR_CUDA;
+  static int cache[64];  // 0 unknown, 1 ok, 2 bad
+  if (dev < 64 && cache[dev] == 1) return FA_OK;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? FA_OK : FA_ERR_ARCH;
+}
+
+// [BH][N][d] bf16 as a 3-D tensor (d, N, BH); box 64 x 128 x 1, 128B swizzle.
+int encode_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols), static_cast<cuuint32_t>(fa::kTileM),
+                       1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "null pointer";
+    case FA_ERR_SHAPE: return "invalid shape or scale";
+    case FA_ERR_HEADDIM: return "head dimension must be 64 or 128";
+    case FA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FA_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+long long fa_forward_tile_count(int N, int causal) {
+  if (N < 1) return 0;
+  const long long nq = fa::num_tiles(N, fa::kTileM);
+  const long long nk = fa::num_tiles(N, fa::kTileN);
+  if (!causal) return nq * nk;
+  return nq * (nq + 1) / 2;  // tiles are square: query tile i visits key tiles 0..i
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  const int BH = B * H;
+  fa::TensorMaps maps;
+  if (encode_bhnd(&maps.q, q, BH, N, d) != FA_OK || encode_bhnd(&maps.k, k, BH, N, d) != FA_OK ||
+      encode_bhnd(&maps.v, v, BH, N, d) != FA_OK)
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.tq = &maps.q;
+  a.tk = &maps.k;
+  a.tv = &maps.v;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = log2e_times(scale);
+  a.causal = causal ? 1 : 0;
+  cudaError_t e = fa::launch_forward(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK) return 0;
+  const size_t bytes = static_cast<size_t>(B) * H * N * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                           void* stream) {
+  if (!o || !dO || !D) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(D)) return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  const long long rows = static_cast<long long>(B) * H * N;
+  cudaError_t e = fa::launch_bwd_preprocess(o, dO, D, rows, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+static int bwd_step(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                    const float* D, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                    float scale, int causal, void* stream, bool do_dkdv, bool do_dq) {
+  if (!q || !k || !v || !dO || !lse || !D) return FA_ERR_NULL;
+  if ((do_dkdv && (!dk || !dv)) || (do_dq && !dq)) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(D) || (do_dq && !aligned16(dq)) || (do_dkdv && (!aligned16(dk) || !aligned16(dv))))
+    return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  const int BH = B * H;
+  fa::TensorMaps maps;
+  if (encode_bhnd(&maps.q, q, BH, N, d) != FA_OK || encode_bhnd(&maps.k, k, BH, N, d) != FA_OK ||
+      encode_bhnd(&maps.v, v, BH, N, d) != FA_OK || encode_bhnd(&maps.dO, dO, BH, N, d) != FA_OK)
+    return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  a.tq = &maps.q;
+  a.tk = &maps.k;
+  a.tv = &maps.v;
+  a.tdo = &maps.dO;
+  a.lse = lse;
+  a.D = D;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.scale_log2 = log2e_times(scale);
+  a.causal = causal ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (do_dkdv && fa::launch_bwd_dkdv(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (do_dq && fa::launch_bwd_dq(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
+                     int d, float scale, int causal, void* stream) {
+  return bwd_step(q, k, v, dO, lse, D, nullptr, dk, dv, B, H, N, d, scale, causal, stream, true,
+                  false);
+}
+
+int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                   void* stream) {
+  return bwd_step(q, k, v, dO, lse, D, dq, nullptr, nullptr, B, H, N, d, scale, causal, stream,
+                  false, true);
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!workspace || workspace_bytes < fa_backward_workspace_size(B, H, N, d) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  float* D = static_cast<float*>(workspace);
+  if ((st = fa_backward_preprocess(o, dO, D, B, H, N, d, stream)) != FA_OK) return st;
+  return bwd_step(q, k, v, dO, lse, D, dq, dk, dv, B, H, N, d, scale, causal, stream, true, true);
+}
+
+int fa_get_device_error(void* stream, uint32_t* detail) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t w_fwd = 0, w_bwd = 0;
+  if (fa::fwd_read_clear_error(&w_fwd, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::bwd_read_clear_error(&w_bwd, s) != cudaSuccess) return FA_ERR_CUDA;
+  const uint32_t w = w_fwd ? w_fwd : w_bwd;
+  if (detail) *detail = w;
+  return w ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,616 @@
+// fa_bwd.cu — recompute backward of exact attention for sm_103a.
+//
+// "What is Flash Attention?" 06:52-07:24: P is not stored; it is rebuilt tile
+// by tile from Q, K and the per-row statistic (here lse = m + ln l) with the
+// same tiling loop, trading FLOPs for HBM traffic.  The gradient formulas are
+// the chain rule through the exact definition (the pages state only that the
+// gradients are the same as standard attention's, 08:26):
+//   P = exp(scale * Q K^T - lse),  dV = P^T dO,  dP = dO V^T,
+//   D_i = sum_c dO_ic O_ic,  dS = P o (dP - D),  dQ = scale dS K,
+//   dK = scale dS^T Q.
+//
+// Three kernels:
+//   * bwd_pre:  D = rowsum(dO o O), fp32, HBM-bound.
+//   * bwd_dkdv: one CTA per (batch*head, 128-row key tile).  K_j and V_j stay
+//     in shared memory; 128-row Q_i / dO_i tiles stream through a two-stage
+//     TMA ring.  Scores are computed transposed, S^T = K_j Q_i^T, so the key
+//     row is the TMEM lane: each of 128 threads owns one key row, forms
+//     P^T and dS^T for its row and writes them back as bf16 over S^T / dP^T
+//     in tensor memory, where they are the A operand of
+//     dV += P^T dO_i and dK += dS^T Q_i (accumulators live in TMEM).
+//   * bwd_dq:   one CTA per (batch*head, 128-row query tile).  Q_i, dO_i stay
+//     resident; K_j / V_j stream.  S = Q_i K_j^T and dP = dO_i V_j^T give dS
+//     per query row; dQ += dS K_j accumulates in TMEM.
+// Causal tiles above the diagonal are skipped in both kernels; the mask is
+// applied inside the diagonal tile only.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ unsigned int g_bwd_error;
+
+constexpr int kBwdThreads = 192;
+constexpr int kStages = 2;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// ============================================================ D pre-pass
+// Each group of d/8 consecutive threads owns one row: every thread loads 8
+// bf16 of O and of dO (one 16-byte vector each), forms the partial dot product
+// in fp32, and the group reduces with warp shuffles.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ o,
+                                                         const uint4* __restrict__ dO,
+                                                         float* __restrict__ Dout,
+                                                         long long rows) {
+  constexpr int kPerRow = D / 8;  // threads per row: 8 or 16
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gt / kPerRow;
+  float acc = 0.0f;
+  if (row < rows) {
+    const uint4 a = o[gt];
+    const uint4 b = dO[gt];
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa2 = __bfloat1622float2(pa[e]);
+      const float2 fb2 = __bfloat1622float2(pb[e]);
+      acc = fmaf(fa2.x, fb2.x, acc);
+      acc = fmaf(fa2.y, fb2.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && (gt % kPerRow) == 0) Dout[row] = acc;
+}
+
+// ============================================================ shared pieces
+template <int D>
+struct BwdLayout {
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  // dkdv: K, V resident; Q, dO streamed.  dq: Q, dO resident; K, V streamed.
+  static constexpr uint32_t kRes0 = 0;
+  static constexpr uint32_t kRes1 = kRes0 + kTileBytes;
+  static constexpr uint32_t kStr0 = kRes1 + kTileBytes;                // [stage] tiles
+  static constexpr uint32_t kStr1 = kStr0 + kStages * kTileBytes;      // [stage] tiles
+  static constexpr uint32_t kVec = kStr1 + kStages * kTileBytes;       // lse/D vectors
+  static constexpr uint32_t kBar = kVec + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kSmem = kBar + 256 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCol = 0;     // S (or S^T); P^T bf16 over its first 64 columns
+  static constexpr uint32_t kDPCol = 128;  // dP (or dP^T); dS bf16 over its first 64 columns
+  static constexpr uint32_t kAcc0 = 256;   // dV (dkdv) or dQ (dq)
+  static constexpr uint32_t kAcc1 = 256 + D;  // dK (dkdv)
+};
+
+struct BwdBars {
+  uint64_t res_full;
+  uint64_t str_full[kStages], str_empty[kStages];
+  uint64_t s_full, p_ready, ds_ready;
+  uint64_t vec_ready[2];
+  uint64_t acc_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool bwd_warp_wait(uint64_t* bar, uint32_t parity, BwdBars* b,
+                                              uint32_t code) {
+  bool ok = mbar_wait(bar, parity, &b->abort_flag, &g_bwd_error, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Returns false (uniformly for the CTA) when an earlier CTA of this library
+// already recorded a pipeline timeout: the CTA then exits without work.
+__device__ __forceinline__ bool bwd_init(BwdBars* bars, int warp, uint32_t cols) {
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->res_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->str_full[s], 1);
+      mbar_init(&bars->str_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->vec_ready[0], 128);
+    mbar_init(&bars->vec_ready[1], 128);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = (*static_cast<volatile unsigned int*>(&g_bwd_error) != 0) ? 1 : 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (bars->abort_flag) return false;
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  return true;
+}
+
+__device__ __forceinline__ void bwd_teardown(BwdBars* bars, int warp, uint32_t tmem,
+                                             uint32_t cols) {
+  if (warp == 5) mbar_wait(&bars->drain, 0, &bars->abort_flag, &g_bwd_error, 0x2ff);
+  if (bars->abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, cols);
+  }
+}
+
+// Producer: two resident tiles once, then two streamed tiles per step.
+template <int D>
+__device__ __forceinline__ void bwd_producer(uint8_t* smem, BwdBars* bars,
+                                             const CUtensorMap* r0, const CUtensorMap* r1,
+                                             int res_row0, const CUtensorMap* s0,
+                                             const CUtensorMap* s1, int first_tile, int ntiles,
+                                             int bh) {
+  using L = BwdLayout<D>;
+  tma_prefetch_desc(r0);
+  tma_prefetch_desc(r1);
+  tma_prefetch_desc(s0);
+  tma_prefetch_desc(s1);
+  mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
+#pragma unroll
+  for (int c = 0; c < L::kChunks; ++c) {
+    tma_load_3d(smem + L::kRes0 + c * 16384, r0, &bars->res_full, c * 64, res_row0, bh);
+    tma_load_3d(smem + L::kRes1 + c * 16384, r1, &bars->res_full, c * 64, res_row0, bh);
+  }
+  for (int n = 0; n < ntiles; ++n) {
+    const int s = n % kStages;
+    const uint32_t ph = (n / kStages) & 1;
+    if (!mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101)) break;
+    mbar_arrive_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
+    const int row0 = (first_tile + n) * 128;
+#pragma unroll
+    for (int c = 0; c < L::kChunks; ++c) {
+      tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s], c * 64,
+                  row0, bh);
+      tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s], c * 64,
+                  row0, bh);
+    }
+  }
+}
+
+// K-major operand descriptor for k-step kk of a [128 rows][D] swizzled tile.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand descriptor (rows of the tile are the K dimension) for k-step kk.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + kk * 2048, 16384, 1024);
+}
+
+// Load 128 fp32 columns [col, col+128) of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld128(uint32_t addr, uint32_t (&r)[128]) {
+  tmem_ld32(addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_ld32(addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  tmem_ld32(addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+  tmem_ld32(addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+  tmem_ld_wait();
+  reg_pin(r);
+}
+
+// Store one 128-column TMEM row segment [col, col + D) of fp32 accumulators
+// as bf16 (times `mul`) to global row `dst` (D elements).
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t addr, float mul, __nv_bfloat16* dst,
+                                              bool valid) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(addr + c * 32, r);
+    tmem_ld_wait();
+    reg_pin(r);
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+    if (valid) {
+      uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+  }
+}
+
+// ============================================================ dK / dV
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq,
+                       const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv,
+                       const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
+                       const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk,
+                       __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
+                       float scale_log2) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kBar);
+  float* vec = reinterpret_cast<float*>(smem + L::kVec);  // [2 buf][lse2 | D][128]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nt = (N + 127) / 128;
+  const int kt = static_cast<int>(blockIdx.x / BH);  // causal: key tile 0 is the heaviest
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int k0 = kt * 128;
+  const int i_first = CAUSAL ? kt : 0;
+  const int n_iters = nt - i_first;
+
+  if (!bwd_init(bars, warp, L::kTmemCols)) return;
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    if (lane == 0)
+      bwd_producer<D>(smem, bars, &tk, &tv, k0, &tq, &tdo, i_first, n_iters, bh);
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
+      const uint32_t sK = smem_u32(smem + L::kRes0);
+      const uint32_t sV = smem_u32(smem + L::kRes1);
+      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x201);
+      tc_fence_after_sync();
+      for (int n = 0; ok && n < n_iters; ++n) {
+        const int s = n % kStages;
+        const uint32_t sQ = smem_u32(smem + L::kStr0 + s * L::kTileBytes);
+        const uint32_t sdO = smem_u32(smem + L::kStr1 + s * L::kTileBytes);
+        if (!mbar_wait(&bars->str_full[s], (n / kStages) & 1, &bars->abort_flag, &g_bwd_error,
+                       0x202)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // S^T = K Q_i^T  and  dP^T = V dO_i^T   (both 128 x 128, K = d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kSCol, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kDPCol, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full);
+        // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i MN-major, K = 128 queries)
+        if (!mbar_wait(&bars->p_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x203)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + L::kAcc0, tmem + L::kSCol + kk * 8, mnmajor_desc(sdO, kk), idesc_acc,
+                  (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i   (A = dS^T bf16 in TMEM, B = Q_i MN-major)
+        if (!mbar_wait(&bars->ds_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x204)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + L::kAcc1, tmem + L::kDPCol + kk * 8, mnmajor_desc(sQ, kk), idesc_acc,
+                  (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->str_empty[s]);
+      }
+      if (ok) umma_commit(&bars->acc_done);
+      umma_commit(&bars->drain);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------- per-key-row threads (warps 0-3)
+    const int t = threadIdx.x;
+    const int krow = k0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float* lse_bh = lse + static_cast<size_t>(bh) * N;
+    const float* D_bh = Dvec + static_cast<size_t>(bh) * N;
+    bool ok = true;
+    for (int n = 0; n < n_iters; ++n) {
+      const int it = i_first + n;
+      const int q0 = it * 128;
+      float* lse2_s = vec + (n & 1) * 256;
+      float* D_s = lse2_s + 128;
+      {
+        const int q = q0 + t;
+        lse2_s[t] = (q < N) ? lse_bh[q] * kLog2e : INFINITY;
+        D_s[t] = (q < N) ? D_bh[q] : 0.0f;
+      }
+      // all 128 entries written before anyone reads them (bounded wait)
+      mbar_arrive(&bars->vec_ready[n & 1]);
+      if (!bwd_warp_wait(&bars->vec_ready[n & 1], (n >> 1) & 1, bars, 0x303)) {
+        ok = false;
+        break;
+      }
+      if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x301)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // P^T row of this key: p[c] = 2^(s * scale * log2e - lse_c * log2e)
+      uint32_t pr[128];
+      tmem_ld128(tmem + lane_off + L::kSCol, pr);
+      const bool diag = CAUSAL && (it == kt);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2_s[c]));
+        if (diag && (q0 + c < krow)) p = 0.0f;  // query before key: masked
+        pr[c] = __float_as_uint(p);
+      }
+      {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
+        tmem_st32(tmem + lane_off + L::kSCol, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tmem + lane_off + L::kSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_ready);
+      // dS^T = P^T o (dP^T - D), 32 columns at a time, packed bf16 over dP^T
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kDPCol + c4 * 32, r);
+        tmem_ld_wait();
+        reg_pin(r);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = c4 * 32 + 2 * e;
+          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - D_s[c]);
+          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - D_s[c + 1]);
+          w[e] = pack_bf16x2(ds0, ds1);
+        }
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                tmem + lane_off + L::kDPCol + c4 * 16),
+            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+            "r"(w[14]), "r"(w[15])
+            : "memory");
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->ds_ready);
+    }
+    if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x302)) {
+      tc_fence_after_sync();
+      const bool valid = krow < N;
+      const size_t off = (static_cast<size_t>(bh) * N + (valid ? krow : 0)) * D;
+      store_acc_row<D>(tmem + lane_off + L::kAcc0, 1.0f, dv + off, valid);
+      store_acc_row<D>(tmem + lane_off + L::kAcc1, scale, dk + off, valid);
+    }
+  }
+  bwd_teardown(bars, warp, tmem, L::kTmemCols);
+}
+
+// ============================================================ dQ
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv,
+                     const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
+                     const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
+                     float scale, float scale_log2) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kBar);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nt = (N + 127) / 128;
+  const int qt = nt - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest first
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int q0 = qt * 128;
+  const int n_iters = CAUSAL ? (qt + 1) : nt;
+
+  if (!bwd_init(bars, warp, L::kTmemCols)) return;
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    if (lane == 0) bwd_producer<D>(smem, bars, &tq, &tdo, q0, &tk, &tv, 0, n_iters, bh);
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + L::kRes0);
+      const uint32_t sdO = smem_u32(smem + L::kRes1);
+      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x211);
+      tc_fence_after_sync();
+      for (int n = 0; ok && n < n_iters; ++n) {
+        const int s = n % kStages;
+        const uint32_t sK = smem_u32(smem + L::kStr0 + s * L::kTileBytes);
+        const uint32_t sV = smem_u32(smem + L::kStr1 + s * L::kTileBytes);
+        if (!mbar_wait(&bars->str_full[s], (n / kStages) & 1, &bars->abort_flag, &g_bwd_error,
+                       0x212)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // S = Q_i K_j^T  and  dP = dO_i V_j^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kSCol, kmajor_desc(sQ, kk), kmajor_desc(sK, kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV, kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full);
+        // dQ += dS K_j   (A = dS bf16 in TMEM, B = K_j MN-major, K = 128 keys)
+        if (!mbar_wait(&bars->ds_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + L::kAcc0, tmem + L::kDPCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
+                  (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->str_empty[s]);
+      }
+      if (ok) umma_commit(&bars->acc_done);
+      umma_commit(&bars->drain);
+    }
+    __syncwarp();
+  } else {
+    const int t = threadIdx.x;
+    const int row = q0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const bool rvalid = row < N;
+    const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
+    const float Drow = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;
+    bool ok = true;
+    for (int n = 0; n < n_iters; ++n) {
+      if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t pr[128];
+      tmem_ld128(tmem + lane_off + L::kSCol, pr);
+      const int kv0 = n * 128;
+      const bool need_mask = (CAUSAL && n == n_iters - 1) || (kv0 + 128 > N);
+      const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
+      const int lim_n = N - 1 - kv0;
+      const int lim = need_mask ? (lim_c < lim_n ? lim_c : lim_n) : 0x7fffffff;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2));
+        if (c > lim) p = 0.0f;
+        pr[c] = __float_as_uint(p);
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kDPCol + c4 * 32, r);
+        tmem_ld_wait();
+        reg_pin(r);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = c4 * 32 + 2 * e;
+          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - Drow);
+          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - Drow);
+          w[e] = pack_bf16x2(ds0, ds1);
+        }
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                tmem + lane_off + L::kDPCol + c4 * 16),
+            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+            "r"(w[14]), "r"(w[15])
+            : "memory");
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->ds_ready);
+    }
+    if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x312)) {
+      tc_fence_after_sync();
+      const size_t off = (static_cast<size_t>(bh) * N + (rvalid ? row : 0)) * D;
+      store_acc_row<D>(tmem + lane_off + L::kAcc0, scale, dq + off, rvalid);
+    }
+  }
+  bwd_teardown(bars, warp, tmem, L::kTmemCols);
+}
+
+template <typename Kern>
+cudaError_t prep(Kern k, uint32_t smem) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  constexpr uint32_t smem = BwdLayout<D>::kSmem;
+  cudaError_t e = prep(kern, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = static_cast<long long>((a.N + 127) / 128) * a.BH;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
+      *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
+      static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
+  constexpr uint32_t smem = BwdLayout<D>::kSmem;
+  cudaError_t e = prep(kern, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = static_cast<long long>((a.N + 127) / 128) * a.BH;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
+      *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.BH, a.N,
+      a.scale, a.scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
+                                  cudaStream_t s) {
+  const long long threads = rows * (d / 8);
+  const long long blocks = (threads + 255) / 256;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  if (d == 64)
+    fa_bwd_pre_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), D, rows);
+  else
+    fa_bwd_pre_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), D, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 64) return a.causal ? launch_dkdv_t<64, true>(a, s) : launch_dkdv_t<64, false>(a, s);
+  return a.causal ? launch_dkdv_t<128, true>(a, s) : launch_dkdv_t<128, false>(a, s);
+}
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, s) : launch_dq_t<64, false>(a, s);
+  return a.causal ? launch_dq_t<128, true>(a, s) : launch_dq_t<128, false>(a, s);
+}
+
+cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_bwd_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_bwd_error, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
+}  // namespace fa

@@ -1,0 +1,374 @@
+// fa_fwd.cu — fused exact-attention forward for sm_103a.
+//
+// One CTA computes one 128-row query tile of one (batch, head):
+//   * "What is Flash Attention?" 03:44-04:15 (tiling): the Q tile is loaded
+//     once and stays in shared memory while 128-row K and V tiles stream
+//     through a two-stage ring (TMA, 128-byte swizzle).
+//   * "Atencao exata ..." block-score formula S_ij = Q_i K_j^T / sqrt(d):
+//     tcgen05.mma writes the 128 x 128 fp32 score tile into tensor memory;
+//     two score buffers let S_{j+1} be computed while tile j's softmax runs.
+//   * transcript 04:46-05:17 (online softmax): each softmax thread owns one
+//     query row (= one TMEM lane), keeps the running max m (log2 units of the
+//     scaled scores) and running sum l, writes P~ = 2^(s*scale*log2e - m') as
+//     bf16 back over its score row, and rescales the O accumulator by
+//     alpha = 2^(m - m') when the max grows.  beta of the page is folded in
+//     by exponentiating against the new max directly (same arithmetic as the
+//     "l_new" formula of the mentria page).
+//   * O += P~ V_j is a tcgen05.mma with the P~ operand read from tensor
+//     memory and V from shared memory; O stays in tensor memory (fp32).
+//   * 06:52-07:24: at the end only O = O_acc / l (bf16) and one fp32
+//     statistic per row, lse = (m + log2 l) ln 2, are written.
+//   * causal masking ("FlashAttention ..." talk, optional masking): query
+//     tile i visits key tiles 0..i only; the mask is applied inside the
+//     diagonal tile, so whole tiles above the diagonal are never loaded.
+//
+// Warp roles (192 threads): warps 0-3 softmax / correction / epilogue (thread
+// t <-> query row t <-> TMEM lane t), warp 4 TMA producer, warp 5 TMEM
+// allocator and MMA issuer.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ unsigned int g_fwd_error;
+
+constexpr int kFwdThreads = 192;
+constexpr int kStages = 2;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kChunks = D / 64;
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kTileBytes;
+  static constexpr uint32_t kV = kK + kStages * kTileBytes;
+  static constexpr uint32_t kBar = kV + kStages * kTileBytes;
+  static constexpr uint32_t kSmem = kBar + 256 + 1024;  // + 1024-byte alignment slack
+  static constexpr uint32_t kTmemCols = 512;            // S0, S1, O
+  static constexpr uint32_t kOCol = 256;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_ready[2];
+  uint64_t pv_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, FwdBars* b,
+                                          uint32_t code) {
+  bool ok = mbar_wait(bar, parity, &b->abort_flag, &g_fwd_error, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
+                  float* __restrict__ lse, int BH, int N, float scale_log2) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + L::kBar);
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  const uint32_t sK = smem_u32(smem + L::kK);
+  const uint32_t sV = smem_u32(smem + L::kV);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nq = (N + kTileM - 1) / kTileM;
+  // heaviest query tiles first across all heads
+  const int qt = nq - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int q0 = qt * kTileM;
+  const int nkv = CAUSAL ? (qt + 1) : (N + kTileN - 1) / kTileN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_ready[b], 128);
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->drain, 1);
+    // an earlier CTA already recorded a pipeline timeout: exit without work
+    bars->abort_flag = (*static_cast<volatile unsigned int*>(&g_fwd_error) != 0) ? 1 : 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (bars->abort_flag) return;
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_expect_tx(&bars->q_full, L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_3d(smem + L::kQ + c * 16384, &tq, &bars->q_full, c * 64, q0, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x101)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kK + s * L::kTileBytes + c * 16384, &tk, &bars->k_full[s], c * 64,
+                      j * kTileN, bh);
+        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x102)) break;
+        mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s], c * 64,
+                      j * kTileN, bh);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(&bars->q_full, 0, &bars->abort_flag, &g_fwd_error, 0x201);
+      tc_fence_after_sync();
+      // O += P~_jp V_jp, P~ read from the score buffer of step jp
+      auto issue_pv = [&](int jp) -> bool {
+        const int bp = jp & 1;
+        const int sp = jp % kStages;
+        if (!mbar_wait(&bars->p_ready[bp], (jp >> 1) & 1, &bars->abort_flag, &g_fwd_error, 0x203))
+          return false;
+        if (!mbar_wait(&bars->v_full[sp], (jp / kStages) & 1, &bars->abort_flag, &g_fwd_error,
+                       0x204))
+          return false;
+        tc_fence_after_sync();
+        const uint32_t vbase = sV + sp * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, 16384, 1024);
+          umma_ts(tmem + L::kOCol, tmem + bp * 128 + kk * 8, bdesc, idesc_pv,
+                  (jp > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars->pv_done);
+        umma_commit(&bars->v_empty[sp]);
+        return true;
+      };
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % kStages;
+        const int b = j & 1;
+        if (!mbar_wait(&bars->k_full[s], (j / kStages) & 1, &bars->abort_flag, &g_fwd_error,
+                       0x202)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t kbase = sK + s * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t adesc = sdesc_sw128(sQ + off, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(kbase + off, 16, 1024);
+          umma_ss(tmem + b * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full[b]);
+        umma_commit(&bars->k_empty[s]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(nkv - 1);
+      umma_commit(&bars->drain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps 0-3
+    const int t = threadIdx.x;  // query row within the tile, TMEM lane
+    const int row = q0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float m_run = -INFINITY;  // running max of s * scale * log2(e)
+    float l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j & 1;
+      if (!warp_wait(&bars->s_full[b], (j >> 1) & 1, bars, 0x301)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t sr[128];
+      {
+        uint32_t(&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        uint32_t(&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+        uint32_t(&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+        uint32_t(&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+        const uint32_t base = tmem + lane_off + b * 128;
+        tmem_ld32(base + 0, c0);
+        tmem_ld32(base + 32, c1);
+        tmem_ld32(base + 64, c2);
+        tmem_ld32(base + 96, c3);
+        tmem_ld_wait();
+        reg_pin(sr);
+      }
+      const int kv0 = j * kTileN;
+      const bool need_mask = (CAUSAL && j == nkv - 1) || (kv0 + kTileN > N);
+      if (need_mask) {
+        const int lim_causal = CAUSAL ? (row - kv0) : 0x7fffffff;  // col index <= lim visible
+        const int lim_n = N - 1 - kv0;
+        const int lim = lim_causal < lim_n ? lim_causal : lim_n;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(sr[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      const float m_new = fmaxf(m_run, mx * scale_log2);
+      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+      float sum = 0.0f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
+        sum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      {
+        const uint32_t base = tmem + lane_off + b * 128;
+        tmem_st32(base + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      }
+      const float alpha = ex2_approx(m_run - m_use);  // 0 on the first tile
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      if (j > 0) {
+        // O holds P~_{j-1} V_{j-1} only once that MMA has completed
+        if (!warp_wait(&bars->pv_done, (j - 1) & 1, bars, 0x302)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t addr = tmem + lane_off + L::kOCol + c * 32;
+            tmem_ld32(addr, r);
+            tmem_ld_wait();
+            reg_pin(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(addr, r);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_ready[b]);
+    }
+    // ------------------------------------------------ epilogue
+    if (ok && warp_wait(&bars->pv_done, (nkv - 1) & 1, bars, 0x303)) {
+      tc_fence_after_sync();
+      const float inv_l = 1.0f / l_run;
+      __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kOCol + c * 32, r);
+        tmem_ld_wait();
+        reg_pin(r);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_run + log2f(l_run)) * kLn2;
+    }
+  }
+
+  // ------------------------------------------------ teardown
+  if (warp == 5) {
+    // every MMA this CTA issued has completed before TMEM is released
+    mbar_wait(&bars->drain, 0, &bars->abort_flag, &g_fwd_error, 0x205);
+  }
+  if (bars->abort_flag) {
+    // let any bulk copy already in flight land before the CTA exits
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  constexpr uint32_t smem = FwdLayout<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long nq = (a.N + kTileM - 1) / kTileM;
+  const long long blocks = nq * a.BH;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
+      *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, s) : launch_fwd_t<64, false>(a, s);
+  return a.causal ? launch_fwd_t<128, true>(a, s) : launch_fwd_t<128, false>(a, s);
+}
+
+cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_fwd_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_fwd_error, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
+}  // namespace fa

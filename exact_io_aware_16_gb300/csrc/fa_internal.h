@@ -1,0 +1,61 @@
+// fa_internal.h — host-side declarations shared by the C-ABI layer and the
+// kernel translation units of libfa (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kTileM = 128;   // query rows per tile
+constexpr int kTileN = 128;   // key rows per tile
+constexpr int kBoxCols = 64;  // bf16 columns per 128-byte swizzled TMA box
+
+// A [BH][N][d] bf16 tensor seen by TMA as a 3-D tensor (d, N, BH) with
+// 64 x 128 x 1 boxes and 128-byte swizzle.  Rows past N read as zero.
+struct TensorMaps {
+  CUtensorMap q, k, v, o, dO;
+};
+
+struct FwdArgs {
+  const CUtensorMap* tq;
+  const CUtensorMap* tk;
+  const CUtensorMap* tv;
+  void* o;
+  float* lse;
+  int BH, N, d;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+};
+
+struct BwdArgs {
+  const CUtensorMap* tq;
+  const CUtensorMap* tk;
+  const CUtensorMap* tv;
+  const CUtensorMap* tdo;
+  const float* lse;
+  const float* D;
+  void* dq;
+  void* dk;
+  void* dv;
+  int BH, N, d;
+  float scale;
+  float scale_log2;
+  int causal;
+};
+
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
+                                  cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
+
+// Device error words of each kernel translation unit: read-and-clear.
+cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s);
+cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s);
+
+// Tile counts (host-side mirror of the kernels' loop bounds).
+inline int num_tiles(int N, int tile) { return (N + tile - 1) / tile; }
+
+}  // namespace fa

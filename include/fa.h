@@ -1,0 +1,140 @@
+/*
+ * fa.h — C ABI of the exact IO-aware attention library (libfa.so, sm_103a).
+ *
+ * Exact scaled-dot-product attention O = softmax(scale * Q K^T) V computed
+ * tile by tile with an online softmax, so the N x N score and probability
+ * matrices never reach device memory, plus the recompute backward that
+ * rebuilds probability tiles from Q, K and the stored per-row logsumexp.
+ *
+ * Sources:
+ *  - "What is Flash Attention?" (Data Science in your pocket), transcript
+ *    02:38-03:44 (one fused kernel, only O is written), 03:44-04:15 (tiling:
+ *    a Q block stays on chip while K/V blocks stream through), 04:46-05:17
+ *    (running max m and sum l with rescaling of the output accumulator),
+ *    06:52-07:24 (keep O and two statistics per row; recompute P block by
+ *    block in the backward pass).
+ *  - "Atencao exata, acelerada por nunca escrever a grade gigante."
+ *    (mentria.ai): block scores S_ij = Q_i K_j^T / sqrt(d); safe softmax;
+ *    o_flash = o_exact.
+ *  - "FlashAttention: fast and memory-efficient exact attention with
+ *    IO-awareness" (talk): optional masking before the softmax.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors q, k, v, o, dO, dq, dk, dv are bf16, contiguous, layout
+ *    [B][H][N][d] (row-major; element (b,h,i,c) at ((b*H + h)*N + i)*d + c).
+ *  - lse and the D pre-pass are fp32 [B][H][N].  lse_i = m_i + ln l_i is the
+ *    natural-log logsumexp of row i of the SCALED scores scale*q_i.k_j.
+ *  - causal != 0 masks key j for query i when j > i (square, top-left
+ *    aligned); masked scores are -inf before the softmax.
+ *  - d must be 64 or 128; B, H, N >= 1; B*H*N*d < 2^31; scale > 0 and finite.
+ *  - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.
+ *    The library allocates no device memory in these calls.  In-place use
+ *    (an output aliasing an input) is undefined.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream).  They return after the kernels are enqueued.  Argument errors
+ *    are returned immediately and nothing is launched.  A launch failure
+ *    returns FA_ERR_CUDA.  A device-side pipeline timeout is reported later
+ *    by fa_get_device_error().
+ *  - Only sm_103 (GB300) devices are accepted (FA_ERR_ARCH otherwise).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = -1,           /* a required pointer is NULL */
+  FA_ERR_SHAPE = -2,          /* B, H or N < 1, sizes overflow, or bad scale */
+  FA_ERR_HEADDIM = -3,        /* d not in {64, 128} */
+  FA_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned */
+  FA_ERR_ARCH = -5,           /* current device is not sm_103 */
+  FA_ERR_WORKSPACE = -6,      /* workspace missing or too small */
+  FA_ERR_CUDA = -7,           /* a CUDA runtime / driver call failed */
+  FA_ERR_DEVICE_TIMEOUT = -8  /* a kernel pipeline wait timed out */
+} fa_status;
+
+/*
+ * Forward pass.  q, k, v: [B][H][N][d] bf16 inputs.  o: [B][H][N][d] bf16
+ * output.  lse: [B][H][N] fp32 output (logsumexp of the scaled scores).
+ * Follows the fused tiled forward with the online softmax ("What is Flash
+ * Attention?", 02:38-06:52).  The score matrix is never written to memory.
+ */
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs: the D pre-pass,
+ * 4 * B * H * N bytes (fp32 [B][H][N]), rounded up to 256.  Returns 0 when
+ * the shape is invalid.
+ */
+size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation ("What is Flash Attention?", 06:52-07:24:
+ * P is rebuilt block by block from Q, K and the per-row statistics).
+ * Inputs: q, k, v, o (the forward output), dO (gradient of o), all bf16
+ * [B][H][N][d]; lse fp32 [B][H][N] from fa_forward.  Outputs dq, dk, dv
+ * bf16 [B][H][N][d].  workspace: caller-owned device memory of at least
+ * fa_backward_workspace_size() bytes, 256-byte aligned; its contents on entry
+ * do not matter.  Gradients are those of the chain rule through the exact
+ * definition: dV = P^T dO, dP = dO V^T, D_i = rowsum(dO o O)_i,
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ */
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * D pre-pass alone: D[b,h,i] = sum_c dO[b,h,i,c] * o[b,h,i,c] in fp32
+ * (bf16 inputs, fp32 output [B][H][N]).  fa_backward runs it itself; it is
+ * exported so that the step can be checked and timed on its own.
+ */
+int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                           void* stream);
+
+/*
+ * The two recompute kernels of fa_backward, callable one at a time (for
+ * timing and checking each step; fa_backward runs the D pre-pass and then
+ * both).  D is the fp32 [B][H][N] output of fa_backward_preprocess.
+ *  - fa_backward_dkdv: for each 128-row key tile, streams query tiles,
+ *    rebuilds P^T from lse, and writes dk = scale * dS^T Q and dv = P^T dO.
+ *  - fa_backward_dq: for each 128-row query tile, streams key tiles,
+ *    rebuilds P and dS and writes dq = scale * dS K.
+ * Arguments and errors as for fa_backward.
+ */
+int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                     const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
+                     int d, float scale, int causal, void* stream);
+int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                   void* stream);
+
+/*
+ * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
+ * this library timed out in a pipeline wait since the last call (and clears
+ * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.
+ * *detail (may be NULL) receives the raw device record (0 when clean).
+ */
+int fa_get_device_error(void* stream, uint32_t* detail);
+
+/* Static description of a status code. */
+const char* fa_status_string(int status);
+
+/*
+ * Number of (query tile, key tile) pairs the forward pass visits for one
+ * (batch, head): nq * nk without masking, sum over query tiles i of (i + 1)
+ * with the causal mask (tiles of 128 x 128).  Host-only arithmetic.
+ */
+long long fa_forward_tile_count(int N, int causal);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

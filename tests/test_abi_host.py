@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point declared in include/fa.h, and rejects bad arguments with
+the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_16_gb300 as fa
+from exact_io_aware_16_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("fa_forward", "fa_backward", "fa_backward_workspace_size",
+                 "fa_get_device_error", "fa_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation returns first
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+        causal=0):
+    return lib.fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+def test_forward_validation(lib):
+    assert fwd(lib, q=None) == -1
+    assert fwd(lib, lse=None) == -1
+    assert fwd(lib, N=0) == -2
+    assert fwd(lib, B=0) == -2
+    assert fwd(lib, H=-1) == -2
+    assert fwd(lib, d=96) == -3
+    assert fwd(lib, d=256) == -3
+    assert fwd(lib, scale=0.0) == -2
+    assert fwd(lib, scale=-1.0) == -2
+    assert fwd(lib, scale=float("inf")) == -2
+    assert fwd(lib, B=1 << 15, H=1 << 15, N=4, d=64) == -2  # B*H*N*d >= 2^31
+    assert fwd(lib, q=FAKE + 8) == -4
+    assert fwd(lib, o=FAKE + 2) == -4
+    assert fwd(lib, lse=FAKE + 4) == -4
+
+
+def bwd(lib, ws=FAKE * 16, ws_bytes=1 << 20, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dO=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, H=1, N=128, d=64, scale=0.125, causal=0)
+    a.update(kw)
+    return lib.fa_backward(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["dq"], a["dk"],
+                           a["dv"], a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"],
+                           ws, ws_bytes, None)
+
+
+def test_backward_validation(lib):
+    assert bwd(lib, dO=None) == -1
+    assert bwd(lib, dv=None) == -1
+    assert bwd(lib, N=0) == -2
+    assert bwd(lib, d=32) == -3
+    assert bwd(lib, ws=None) == -6
+    assert bwd(lib, ws_bytes=100) == -6
+    assert bwd(lib, ws=FAKE * 16 + 16) == -6  # workspace must be 256-byte aligned
+    assert bwd(lib, dk=FAKE + 4) == -4
+
+
+def test_workspace_size_is_linear_in_n(lib):
+    f = lib.fa_backward_workspace_size
+    assert f(1, 1, 0, 64) == 0
+    assert f(1, 1, 128, 96) == 0
+    for N in (1000, 4096, 8192, 16384):
+        assert f(2, 16, N, 128) == ((2 * 16 * N * 4 + 255) // 256) * 256
+    assert f(2, 16, 16384, 128) == 2 * f(2, 16, 8192, 128)
+
+
+def test_tile_count(lib):
+    for N in (1, 127, 128, 129, 1000, 8192):
+        nt = -(-N // 128)
+        assert fa.fa_forward_tile_count(N, False) == nt * nt
+        assert fa.fa_forward_tile_count(N, True) == sum(i + 1 for i in range(nt))
+
+
+def test_status_strings(lib):
+    for s in range(-8, 1):
+        assert fa.fa_status_string(s) not in ("", "unknown status")
+    assert fa.fa_status_string(-99) == "unknown status"
+
+
+def test_binding_has_no_fallback(monkeypatch, tmp_path):
+    # With the library path pointing nowhere, the binding raises instead of
+    # computing anything on another path.
+    from exact_io_aware_16_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "_LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _binding.library()
