@@ -2,7 +2,7 @@
 """Benchmark of exact attention fwd+bwd on GB300 through the C ABI of libfa.
 
 One step = one forward pass (fa_forward) and one backward pass (D pre-pass,
-dK/dV kernel, dQ kernel) over one batch of seeded synthetic bf16 inputs
+dQ kernel, dK/dV kernel) over one batch of seeded synthetic bf16 inputs
 already resident in device memory.  The default workload is causal attention
 with B=2, H=16, N=8192, d=128, scale 1/sqrt(d) (the long-context case where
 the FLOP target applies).
@@ -215,7 +215,7 @@ def run_ours(args, world, rank, local):
     D = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
-    names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
+    names = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
 
     def step(ev=None):
         fa.fa_forward(q, k, v, causal=causal, scale=scale, o=o, lse=lse, stream=stream)
@@ -224,11 +224,11 @@ def run_ours(args, world, rank, local):
         fa.fa_backward_preprocess(o, dO, D, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, scale=scale, dk=dk, dv=dv,
-                            stream=stream)
+        fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, scale=scale, dq=dq, stream=stream)
         if ev is not None:
             ev[3].record(stream)
-        fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, scale=scale, dq=dq, stream=stream)
+        fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, scale=scale, dk=dk, dv=dv,
+                            stream=stream)
         if ev is not None:
             ev[4].record(stream)
 

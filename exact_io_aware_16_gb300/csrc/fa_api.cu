@@ -155,7 +155,7 @@ int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H
 }
 
 static int bwd_step(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                    const float* D, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                    float* D, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                     float scale, int causal, void* stream, bool do_dkdv, bool do_dq) {
   if (!q || !k || !v || !dO || !lse || !D) return FA_ERR_NULL;
   if ((do_dkdv && (!dk || !dv)) || (do_dq && !dq)) return FA_ERR_NULL;
@@ -188,20 +188,22 @@ static int bwd_step(const void* q, const void* k, const void* v, const void* dO,
   a.scale_log2 = log2e_times(scale);
   a.causal = causal ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (do_dkdv && fa::launch_bwd_dkdv(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  // dQ first: it refines D in place (exact D = sum_j P_ij dP_ij), which the
+  // dK / dV kernel then reads.
   if (do_dq && fa::launch_bwd_dq(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (do_dkdv && fa::launch_bwd_dkdv(a, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 
 int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO,
                      const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
                      int d, float scale, int causal, void* stream) {
-  return bwd_step(q, k, v, dO, lse, D, nullptr, dk, dv, B, H, N, d, scale, causal, stream, true,
-                  false);
+  return bwd_step(q, k, v, dO, lse, const_cast<float*>(D), nullptr, dk, dv, B, H, N, d, scale,
+                  causal, stream, true, false);
 }
 
 int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                   const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                   float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
                    void* stream) {
   return bwd_step(q, k, v, dO, lse, D, dq, nullptr, nullptr, B, H, N, d, scale, causal, stream,
                   false, true);

@@ -407,12 +407,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ============================================================ dQ
+// dS needs D_i before the loop over key tiles has seen the whole row, so the
+// loop uses the pre-pass estimate D~_i = rowsum(dO o O) (O stored in bf16) and
+// accumulates, alongside dQ~ = scale sum_j P_ij (dP_ij - D~_i) k_j, the exact
+// definition D_i = sum_j P_ij dP_ij (fp32) and B_i = sum_j P_ij k_j (one more
+// MMA).  The epilogue corrects dQ = dQ~ - scale (D_i - D~_i) B_i, which removes
+// the error that bf16 rounding of O puts into D~, and writes D_i back over
+// D~_i for the dK/dV kernel that runs next.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv,
                      const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
-                     const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
+                     float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
                      float scale, float scale_log2) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -426,6 +433,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int q0 = qt * 128;
   const int n_iters = CAUSAL ? (qt + 1) : nt;
+  constexpr uint32_t kDQ = L::kAcc0;  // dQ~ accumulator
+  constexpr uint32_t kB = L::kAcc1;   // B = P K accumulator
 
   if (!bwd_init(bars, warp, L::kTmemCols)) return;
   const uint32_t tmem = bars->tmem_base;
@@ -461,7 +470,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV, kk), idesc_s,
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full);
-        // dQ += dS K_j   (A = dS bf16 in TMEM, B = K_j MN-major, K = 128 keys)
+        // B += P K_j   (A = P bf16 in TMEM over S, B = K_j MN-major)
+        if (!mbar_wait(&bars->p_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x214)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kB, tmem + L::kSCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
+                  (n > 0 || kk > 0) ? 1u : 0u);
+        // dQ~ += dS~ K_j   (A = dS~ bf16 in TMEM over dP)
         if (!mbar_wait(&bars->ds_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
           ok = false;
           break;
@@ -469,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + L::kAcc0, tmem + L::kDPCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
+          umma_ts(tmem + kDQ, tmem + L::kDPCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
                   (n > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->str_empty[s]);
       }
@@ -483,7 +502,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const bool rvalid = row < N;
     const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
-    const float Drow = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;
+    const float Dt = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;  // D~
+    float Dx = 0.0f;  // exact D = sum_j P_ij dP_ij
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {
@@ -504,6 +524,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (c > lim) p = 0.0f;
         pr[c] = __float_as_uint(p);
       }
+      {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
+        tmem_st32(tmem + lane_off + L::kSCol, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tmem + lane_off + L::kSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_ready);
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t r[32];
@@ -514,9 +545,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = c4 * 32 + 2 * e;
-          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - Drow);
-          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - Drow);
-          w[e] = pack_bf16x2(ds0, ds1);
+          const float p0 = __uint_as_float(pr[c]), p1 = __uint_as_float(pr[c + 1]);
+          const float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
+          Dx = fmaf(p0, dp0, Dx);
+          Dx = fmaf(p1, dp1, Dx);
+          w[e] = pack_bf16x2(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
         }
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -533,8 +566,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x312)) {
       tc_fence_after_sync();
+      const float corr = Dx - Dt;
       const size_t off = (static_cast<size_t>(bh) * N + (rvalid ? row : 0)) * D;
-      store_acc_row<D>(tmem + lane_off + L::kAcc0, scale, dq + off, rvalid);
+      __nv_bfloat16* dst = dq + off;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + kDQ + c * 32, a);
+        tmem_ld32(tmem + lane_off + kB + c * 32, b);
+        tmem_ld_wait();
+        reg_pin(a);
+        reg_pin(b);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = scale * fmaf(-corr, __uint_as_float(b[2 * e]), __uint_as_float(a[2 * e]));
+          const float x1 =
+              scale * fmaf(-corr, __uint_as_float(b[2 * e + 1]), __uint_as_float(a[2 * e + 1]));
+          w[e] = pack_bf16x2(x0, x1);
+        }
+        if (rvalid) {
+          uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (rvalid) Dvec[static_cast<size_t>(bh) * N + row] = Dx;
     }
   }
   bwd_teardown(bars, warp, tmem, L::kTmemCols);

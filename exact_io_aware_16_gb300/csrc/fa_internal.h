@@ -35,7 +35,7 @@ struct BwdArgs {
   const CUtensorMap* tv;
   const CUtensorMap* tdo;
   const float* lse;
-  const float* D;
+  float* D;  // D~ in; the dQ kernel overwrites it with the exact D
   void* dq;
   void* dk;
   void* dv;

@@ -83,8 +83,10 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  * bf16 [B][H][N][d].  workspace: caller-owned device memory of at least
  * fa_backward_workspace_size() bytes, 256-byte aligned; its contents on entry
  * do not matter.  Gradients are those of the chain rule through the exact
- * definition: dV = P^T dO, dP = dO V^T, D_i = rowsum(dO o O)_i,
- * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ * definition: dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij (which equals
+ * rowsum(dO o O)_i), dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ * Kernels: the D pre-pass (from the bf16 O), the dQ kernel (which also
+ * leaves the exact D in the workspace) and the dK/dV kernel.
  */
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
@@ -100,20 +102,26 @@ int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H
 
 /*
  * The two recompute kernels of fa_backward, callable one at a time (for
- * timing and checking each step; fa_backward runs the D pre-pass and then
- * both).  D is the fp32 [B][H][N] output of fa_backward_preprocess.
- *  - fa_backward_dkdv: for each 128-row key tile, streams query tiles,
- *    rebuilds P^T from lse, and writes dk = scale * dS^T Q and dv = P^T dO.
+ * timing and checking each step).  fa_backward runs the D pre-pass, then
+ * fa_backward_dq, then fa_backward_dkdv; separate callers must keep that
+ * order on one stream.
  *  - fa_backward_dq: for each 128-row query tile, streams key tiles,
- *    rebuilds P and dS and writes dq = scale * dS K.
+ *    rebuilds P and dS and writes dq = scale * dS K.  D (fp32 [B][H][N]) is
+ *    read and written: it enters as the pre-pass estimate rowsum(dO o O),
+ *    whose O is bf16-rounded, and leaves as the exact sum_j P_ij dP_ij
+ *    accumulated in fp32 while the row is swept; dq is corrected for the
+ *    difference (dq -= scale * (D - D~) * P K).
+ *  - fa_backward_dkdv: for each 128-row key tile, streams query tiles,
+ *    rebuilds P^T from lse, and writes dk = scale * dS^T Q and dv = P^T dO,
+ *    using the D left by fa_backward_dq.
  * Arguments and errors as for fa_backward.
  */
+int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                   void* stream);
 int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO,
                      const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
                      int d, float scale, int causal, void* stream);
-int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                   const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
-                   void* stream);
 
 /*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of

@@ -49,8 +49,8 @@ def test_outputs_stay_in_bounds(fa, N, d, causal):
     kb, dk = guarded((B, H, N, d), torch.bfloat16, dev)
     vb, dv = guarded((B, H, N, d), torch.bfloat16, dev)
     qb, dq = guarded((B, H, N, d), torch.bfloat16, dev)
-    fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, dk=dk, dv=dv)
     fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, dq=dq)
+    fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert fa.fa_get_device_error()[0] == 0
     for name, b in (("o", ob), ("lse", lb), ("D", Db), ("dk", kb), ("dv", vb), ("dq", qb)):
