@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     fa_backward,
     fa_backward_dkdv,
     fa_backward_dq,
+    fa_backward_noalloc,
     fa_backward_preprocess,
     fa_backward_workspace_size,
     fa_forward,
@@ -23,7 +24,7 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "FaError", "fa_forward", "fa_backward", "fa_backward_preprocess", "fa_backward_dkdv",
-    "fa_backward_dq",
+    "fa_backward_dq", "fa_backward_noalloc",
     "fa_backward_workspace_size", "fa_forward_tile_count", "fa_get_device_error",
     "fa_status_string", "library", "library_path",
 ]

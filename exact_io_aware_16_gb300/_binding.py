@@ -56,6 +56,9 @@ def library():
         lib.fa_backward.restype = i
         lib.fa_backward_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.fa_backward_preprocess.restype = i
+        lib.fa_backward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i,
+                                             vp]
+        lib.fa_backward_noalloc.restype = i
         lib.fa_backward_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_backward_dkdv.restype = i
         lib.fa_backward_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -162,6 +165,27 @@ def fa_backward(q, k, v, o, dO, lse, causal: bool = False, scale: float | None =
                                ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward")
+    return dq, dk, dv
+
+
+def fa_backward_noalloc(q, k, v, o, dO, lse, causal: bool = False, scale: float | None = None,
+                        dq=None, dk=None, dv=None, stream=None):
+    """fa_backward for callers that cannot allocate: the library's built-in
+    8 MiB workspace replaces the caller's (B*H*N <= 2,097,152)."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = library().fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                       int(bool(causal)),
+                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_noalloc")
     return dq, dk, dv
 
 

@@ -93,6 +93,34 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
                 float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Largest B*H*N that fa_backward_noalloc accepts (its built-in workspace
+ * holds one fp32 per row: 8 MiB).
+ */
+#define FA_NOALLOC_MAX_ROWS 2097152
+
+/*
+ * fa_backward without a caller-provided workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- a host runtime that hands all device memory to its own
+ * pool at start-up, a plugin-style interface that passes only tensors and a
+ * stream, or a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation.  Arguments and results are those of fa_backward
+ * minus the workspace; the call itself allocates nothing.
+ *  - The workspace is a fixed 8 MiB array inside the library, held by every
+ *    GPU that loads the library until the process exits.
+ *  - B*H*N > FA_NOALLOC_MAX_ROWS returns FA_ERR_WORKSPACE; nothing runs.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array.  Calls on one stream (or otherwise
+ *    ordered) are safe; calls whose kernels overlap on the GPU race on it.
+ *    No state carries over between calls: the array is fully rewritten
+ *    before it is read.
+ */
+int fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, float scale, int causal, void* stream);
+
+/*
  * D pre-pass alone: D[b,h,i] = sum_c dO[b,h,i,c] * o[b,h,i,c] in fp32
  * (bf16 inputs, fp32 output [B][H][N]).  fa_backward runs it itself; it is
  * exported so that the step can be checked and timed on its own.
