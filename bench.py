@@ -50,6 +50,27 @@ def read_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, or None
+    when there is none for this workload or the kernel source changed since."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+        if not rec or rec["workload"] != workload:
+            return None
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest() != rec["source_sha256"]:
+            return None
+        return rec["read_bytes"] + rec["write_bytes"]
+    except Exception:
+        return None
+
+
 def flops(w, causal):
     base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
     return 4.0 * base, 10.0 * base
@@ -290,7 +311,8 @@ def run_ours(args, world, rank, local):
     else:
         ach = kflops[dom] / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": captured_traffic(dom, w.name) if causal == w.causal[0] else None,
                 "peak_kind": f"{peak_kind} bf16 ({peak_src})"}
     roof["ms_per_launch"] = dom_ms
 
