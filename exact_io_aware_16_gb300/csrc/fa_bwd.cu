@@ -36,7 +36,7 @@ namespace {
 
 __device__ unsigned int g_bwd_error;
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 constexpr int kStages = 2;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -72,6 +72,17 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
 }
 
 // ============================================================ shared pieces
+// Warp roles of both recompute kernels (320 threads):
+//   warps 0-7  two compute warpgroups; warpgroup g owns score columns
+//              [64g, 64g+64) of every row, thread t of a warpgroup owns TMEM
+//              lane (row) t, so the 128 columns of a tile are processed by two
+//              warps per SM sub-partition;
+//   warp 8     TMA producer;
+//   warp 9     TMEM allocator and MMA issuer.
+constexpr int kComputeThreads = 256;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+
 template <int D>
 struct BwdLayout {
   static constexpr int kChunks = D / 64;
@@ -85,17 +96,17 @@ struct BwdLayout {
   static constexpr uint32_t kBar = kVec + 2 * 2 * 128 * 4;
   static constexpr uint32_t kSmem = kBar + 256 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol = 0;     // S (or S^T); P^T bf16 over its first 64 columns
-  static constexpr uint32_t kDPCol = 128;  // dP (or dP^T); dS bf16 over its first 64 columns
-  static constexpr uint32_t kAcc0 = 256;   // dV (dkdv) or dQ (dq)
-  static constexpr uint32_t kAcc1 = 256 + D;  // dK (dkdv)
+  static constexpr uint32_t kSCol = 0;     // S (or S^T); P bf16 packed inside each half
+  static constexpr uint32_t kDPCol = 128;  // dP (or dP^T); dS bf16 packed inside each half
+  static constexpr uint32_t kAcc0 = 256;   // dV (dkdv) or dQ~ (dq)
+  static constexpr uint32_t kAcc1 = 256 + D;  // dK (dkdv) or B = P K (dq)
 };
 
 struct BwdBars {
   uint64_t res_full;
   uint64_t str_full[kStages], str_empty[kStages];
-  uint64_t s_full, p_ready, ds_ready;
-  uint64_t vec_ready[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready;
+  uint64_t dx_ready;
   uint64_t acc_done;
   uint64_t drain;
   uint32_t tmem_base;
@@ -118,10 +129,10 @@ __device__ __forceinline__ bool bwd_init(BwdBars* bars, int warp, uint32_t cols)
       mbar_init(&bars->str_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_ready, 128);
-    mbar_init(&bars->ds_ready, 128);
-    mbar_init(&bars->vec_ready[0], 128);
-    mbar_init(&bars->vec_ready[1], 128);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kComputeThreads);
+    mbar_init(&bars->ds_ready, kComputeThreads);
+    mbar_init(&bars->dx_ready, kComputeThreads);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = (*static_cast<volatile unsigned int*>(&g_bwd_error) != 0) ? 1 : 0;
@@ -129,7 +140,7 @@ __device__ __forceinline__ bool bwd_init(BwdBars* bars, int warp, uint32_t cols)
   }
   __syncthreads();
   if (bars->abort_flag) return false;
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, cols);
     tmem_relinquish();
   }
@@ -141,7 +152,7 @@ __device__ __forceinline__ bool bwd_init(BwdBars* bars, int warp, uint32_t cols)
 
 __device__ __forceinline__ void bwd_teardown(BwdBars* bars, int warp, uint32_t tmem,
                                              uint32_t cols) {
-  if (warp == 5) mbar_wait(&bars->drain, 0, &bars->abort_flag, &g_bwd_error, 0x2ff);
+  if (warp == kMmaWarp) mbar_wait(&bars->drain, 0, &bars->abort_flag, &g_bwd_error, 0x2ff);
   if (bars->abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 200000ull) {
@@ -149,43 +160,66 @@ __device__ __forceinline__ void bwd_teardown(BwdBars* bars, int warp, uint32_t t
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, cols);
   }
 }
 
-// Producer: two resident tiles once, then two streamed tiles per step.
+// Producer (the whole TMA warp): two resident tiles once, then two streamed
+// tiles per step.  When `lse` is given (dK/dV kernel), the warp also stages
+// the streamed query tile's lse * log2(e) (+inf past N) and D (0 past N) in
+// shared memory before lane 0 arrives on the stage's barrier, so they travel
+// with the tiles.
 template <int D>
 __device__ __forceinline__ void bwd_producer(uint8_t* smem, BwdBars* bars,
                                              const CUtensorMap* r0, const CUtensorMap* r1,
                                              int res_row0, const CUtensorMap* s0,
                                              const CUtensorMap* s1, int first_tile, int ntiles,
-                                             int bh) {
+                                             int bh, const float* lse_bh, const float* D_bh,
+                                             int N) {
   using L = BwdLayout<D>;
-  tma_prefetch_desc(r0);
-  tma_prefetch_desc(r1);
-  tma_prefetch_desc(s0);
-  tma_prefetch_desc(s1);
-  mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
+  const int lane = static_cast<int>(lane_id());
+  if (lane == 0) {
+    tma_prefetch_desc(r0);
+    tma_prefetch_desc(r1);
+    tma_prefetch_desc(s0);
+    tma_prefetch_desc(s1);
+    mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
 #pragma unroll
-  for (int c = 0; c < L::kChunks; ++c) {
-    tma_load_3d(smem + L::kRes0 + c * 16384, r0, &bars->res_full, c * 64, res_row0, bh);
-    tma_load_3d(smem + L::kRes1 + c * 16384, r1, &bars->res_full, c * 64, res_row0, bh);
+    for (int c = 0; c < L::kChunks; ++c) {
+      tma_load_3d(smem + L::kRes0 + c * 16384, r0, &bars->res_full, c * 64, res_row0, bh);
+      tma_load_3d(smem + L::kRes1 + c * 16384, r1, &bars->res_full, c * 64, res_row0, bh);
+    }
   }
   for (int n = 0; n < ntiles; ++n) {
     const int s = n % kStages;
     const uint32_t ph = (n / kStages) & 1;
-    if (!mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101)) break;
-    mbar_arrive_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
+    bool ok = mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101);
+    if (!__all_sync(0xffffffffu, ok)) break;
     const int row0 = (first_tile + n) * 128;
+    if (lse_bh != nullptr) {
+      float* vec = reinterpret_cast<float*>(smem + L::kVec) + s * 256;  // [lse2 | D]
 #pragma unroll
-    for (int c = 0; c < L::kChunks; ++c) {
-      tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s], c * 64,
-                  row0, bh);
-      tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s], c * 64,
-                  row0, bh);
+      for (int e = 0; e < 4; ++e) {
+        const int i = lane + 32 * e;
+        const int q = row0 + i;
+        vec[i] = (q < N) ? lse_bh[q] * kLog2e : INFINITY;
+        vec[128 + i] = (q < N) ? D_bh[q] : 0.0f;
+      }
+      __syncwarp();
     }
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s],
+                    c * 64, row0, bh);
+        tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s],
+                    c * 64, row0, bh);
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -197,24 +231,37 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, 16384, 1024);
 }
+// TMEM column of k-step kk (16 score columns) of a bf16 operand packed inside
+// the two 64-column halves of a 128-column fp32 region: half g holds score
+// columns [64g, 64g+64) packed in its first 32 columns.
+__device__ __forceinline__ uint32_t packed_a_col(int kk) {
+  return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+}
 
-// Load 128 fp32 columns [col, col+128) of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld128(uint32_t addr, uint32_t (&r)[128]) {
+// Load 64 fp32 columns [addr, addr+64) of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, uint32_t (&r)[64]) {
   tmem_ld32(addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
   tmem_ld32(addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-  tmem_ld32(addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-  tmem_ld32(addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
   tmem_ld_wait();
   reg_pin(r);
 }
 
-// Store one 128-column TMEM row segment [col, col + D) of fp32 accumulators
-// as bf16 (times `mul`) to global row `dst` (D elements).
-template <int D>
-__device__ __forceinline__ void store_acc_row(uint32_t addr, float mul, __nv_bfloat16* dst,
-                                              bool valid) {
+__device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&w)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(addr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+      "r"(w[15])
+      : "memory");
+}
+
+// Store 64 fp32 accumulator columns [addr, addr+64) of this lane as bf16
+// (times `mul`) to 64 consecutive elements at dst.
+__device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bfloat16* dst,
+                                               bool valid) {
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t r[32];
     tmem_ld32(addr + c * 32, r);
     tmem_ld_wait();
@@ -246,12 +293,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kBar);
-  float* vec = reinterpret_cast<float*>(smem + L::kVec);  // [2 buf][lse2 | D][128]
+  const float* vec = reinterpret_cast<const float*>(smem + L::kVec);  // [stage][lse2 | D][128]
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
-  const int kt = static_cast<int>(blockIdx.x / BH);  // causal: key tile 0 is the heaviest
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // head-major order (the key tiles of one head run together and share its
+  // Q / dO tiles in L2); within a head, key tile 0 (the heaviest when causal)
+  // first
+  const int bh = static_cast<int>(blockIdx.x / nt);
+  const int kt = static_cast<int>(blockIdx.x % nt);
   const int k0 = kt * 128;
   const int i_first = CAUSAL ? kt : 0;
   const int n_iters = nt - i_first;
@@ -259,39 +309,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (!bwd_init(bars, warp, L::kTmemCols)) return;
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 4) {
-    if (lane == 0)
-      bwd_producer<D>(smem, bars, &tk, &tv, k0, &tq, &tdo, i_first, n_iters, bh);
-    __syncwarp();
-  } else if (warp == 5) {
+  if (warp == kTmaWarp) {
+    bwd_producer<D>(smem, bars, &tk, &tv, k0, &tq, &tdo, i_first, n_iters, bh,
+                    lse + static_cast<size_t>(bh) * N, Dvec + static_cast<size_t>(bh) * N, N);
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
       const uint32_t sK = smem_u32(smem + L::kRes0);
       const uint32_t sV = smem_u32(smem + L::kRes1);
-      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x201);
-      tc_fence_after_sync();
-      for (int n = 0; ok && n < n_iters; ++n) {
-        const int s = n % kStages;
-        const uint32_t sQ = smem_u32(smem + L::kStr0 + s * L::kTileBytes);
-        const uint32_t sdO = smem_u32(smem + L::kStr1 + s * L::kTileBytes);
-        if (!mbar_wait(&bars->str_full[s], (n / kStages) & 1, &bars->abort_flag, &g_bwd_error,
-                       0x202)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // S^T = K Q_i^T  and  dP^T = V dO_i^T   (both 128 x 128, K = d)
+      auto sQ = [&](int n) { return smem_u32(smem + L::kStr0 + (n % kStages) * L::kTileBytes); };
+      auto sdO = [&](int n) { return smem_u32(smem + L::kStr1 + (n % kStages) * L::kTileBytes); };
+      // S^T_n = K Q_n^T and dP^T_n = V dO_n^T (both 128 x 128, K = d)
+      auto issue_s = [&](int n) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kSCol, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), idesc_s,
-                  kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kDPCol, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), idesc_s,
+          umma_ss(tmem + L::kSCol, kmajor_desc(sK, kk), kmajor_desc(sQ(n), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full);
-        // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i MN-major, K = 128 queries)
+      };
+      auto issue_dp = [&](int n) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kDPCol, kmajor_desc(sV, kk), kmajor_desc(sdO(n), kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->dp_full);
+      };
+      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x201) &&
+                mbar_wait(&bars->str_full[0], 0, &bars->abort_flag, &g_bwd_error, 0x202);
+      tc_fence_after_sync();
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      // order per step: dV_n, S^T_{n+1}, dK_n, dP^T_{n+1}, so that the exps of
+      // step n+1 overlap dK_n and dP^T_{n+1} on the tensor core
+      for (int n = 0; ok && n < n_iters; ++n) {
+        // dV += P^T dO_n   (A = P^T bf16 in TMEM, B = dO_n MN-major, K = 128 queries)
         if (!mbar_wait(&bars->p_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x203)) {
           ok = false;
           break;
@@ -299,9 +353,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + L::kAcc0, tmem + L::kSCol + kk * 8, mnmajor_desc(sdO, kk), idesc_acc,
-                  (n > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i   (A = dS^T bf16 in TMEM, B = Q_i MN-major)
+          umma_ts(tmem + L::kAcc0, tmem + L::kSCol + packed_a_col(kk), mnmajor_desc(sdO(n), kk),
+                  idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+        const bool more = n + 1 < n_iters;
+        if (more) {
+          if (!mbar_wait(&bars->str_full[(n + 1) % kStages], ((n + 1) / kStages) & 1,
+                         &bars->abort_flag, &g_bwd_error, 0x205)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s(n + 1);
+        }
+        // dK += dS^T Q_n   (A = dS^T bf16 in TMEM, B = Q_n MN-major)
         if (!mbar_wait(&bars->ds_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x204)) {
           ok = false;
           break;
@@ -309,87 +373,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + L::kAcc1, tmem + L::kDPCol + kk * 8, mnmajor_desc(sQ, kk), idesc_acc,
-                  (n > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->str_empty[s]);
+          umma_ts(tmem + L::kAcc1, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sQ(n), kk),
+                  idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->str_empty[n % kStages]);
+        if (more) issue_dp(n + 1);
       }
       if (ok) umma_commit(&bars->acc_done);
       umma_commit(&bars->drain);
     }
     __syncwarp();
   } else {
-    // ---------------------------------------- per-key-row threads (warps 0-3)
-    const int t = threadIdx.x;
+    // ---------------------------------------- compute warpgroups (warps 0-7)
+    const int T = threadIdx.x;  // 0..255
+    const int g = T >> 7;       // column half
+    const int t = T & 127;      // key row within the tile = TMEM lane
     const int krow = k0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const float* lse_bh = lse + static_cast<size_t>(bh) * N;
-    const float* D_bh = Dvec + static_cast<size_t>(bh) * N;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t col0 = 64u * g;
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
       const int it = i_first + n;
       const int q0 = it * 128;
-      float* lse2_s = vec + (n & 1) * 256;
-      float* D_s = lse2_s + 128;
-      {
-        const int q = q0 + t;
-        lse2_s[t] = (q < N) ? lse_bh[q] * kLog2e : INFINITY;
-        D_s[t] = (q < N) ? D_bh[q] : 0.0f;
-      }
-      // all 128 entries written before anyone reads them (bounded wait)
-      mbar_arrive(&bars->vec_ready[n & 1]);
-      if (!bwd_warp_wait(&bars->vec_ready[n & 1], (n >> 1) & 1, bars, 0x303)) {
-        ok = false;
-        break;
-      }
+      // lse * log2(e) and D of this query tile, staged with the tiles
+      const float* lse2_s = vec + (n % kStages) * 256;
+      const float* D_s = lse2_s + 128;
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x301)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      // P^T row of this key: p[c] = 2^(s * scale * log2e - lse_c * log2e)
-      uint32_t pr[128];
-      tmem_ld128(tmem + lane_off + L::kSCol, pr);
+      // P^T for this key row and query columns [col0, col0+64)
+      uint32_t pr[64];
+      tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
       const bool diag = CAUSAL && (it == kt);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2_s[c]));
-        if (diag && (q0 + c < krow)) p = 0.0f;  // query before key: masked
+      for (int c = 0; c < 64; ++c) {
+        const int qc = col0 + c;
+        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2_s[qc]));
+        if (diag && (q0 + qc < krow)) p = 0.0f;  // query before key: masked
         pr[c] = __float_as_uint(p);
       }
       {
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 32; ++c)
           pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
-        tmem_st32(tmem + lane_off + L::kSCol, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tmem + lane_off + L::kSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st32(tmem + lane_off + L::kSCol + col0, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars->p_ready);
-      // dS^T = P^T o (dP^T - D), 32 columns at a time, packed bf16 over dP^T
+      if (!bwd_warp_wait(&bars->dp_full, n & 1, bars, 0x304)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // dS^T = P^T o (dP^T - D), 32 columns at a time, packed bf16 in place
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kDPCol + c4 * 32, r);
+        tmem_ld32(tmem + lane_off + L::kDPCol + col0 + c2 * 32, r);
         tmem_ld_wait();
         reg_pin(r);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c = c4 * 32 + 2 * e;
-          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - D_s[c]);
-          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - D_s[c + 1]);
+          const int c = c2 * 32 + 2 * e;
+          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - D_s[col0 + c]);
+          const float ds1 =
+              __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - D_s[col0 + c + 1]);
           w[e] = pack_bf16x2(ds0, ds1);
         }
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-                tmem + lane_off + L::kDPCol + c4 * 16),
-            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
-            "r"(w[14]), "r"(w[15])
-            : "memory");
+        tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -399,8 +454,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       const bool valid = krow < N;
       const size_t off = (static_cast<size_t>(bh) * N + (valid ? krow : 0)) * D;
-      store_acc_row<D>(tmem + lane_off + L::kAcc0, 1.0f, dv + off, valid);
-      store_acc_row<D>(tmem + lane_off + L::kAcc1, scale, dk + off, valid);
+      // d = 128: warpgroup g stores columns [64g, 64g+64) of dV and dK;
+      // d = 64: warpgroup 0 stores dV, warpgroup 1 stores dK
+      if (D == 128) {
+        store_acc_half(tmem + lane_off + L::kAcc0 + col0, 1.0f, dv + off + col0, valid);
+        store_acc_half(tmem + lane_off + L::kAcc1 + col0, scale, dk + off + col0, valid);
+      } else if (g == 0) {
+        store_acc_half(tmem + lane_off + L::kAcc0, 1.0f, dv + off, valid);
+      } else {
+        store_acc_half(tmem + lane_off + L::kAcc1, scale, dk + off, valid);
+      }
     }
   }
   bwd_teardown(bars, warp, tmem, L::kTmemCols);
@@ -426,11 +489,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kBar);
+  float* dx_s = reinterpret_cast<float*>(smem + L::kVec);  // [2 halves][128 rows]
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
-  const int qt = nt - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest first
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // head-major order; within a head the heaviest (last) query tile first
+  const int bh = static_cast<int>(blockIdx.x / nt);
+  const int qt = nt - 1 - static_cast<int>(blockIdx.x % nt);
   const int q0 = qt * 128;
   const int n_iters = CAUSAL ? (qt + 1) : nt;
   constexpr uint32_t kDQ = L::kAcc0;  // dQ~ accumulator
@@ -439,38 +504,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (!bwd_init(bars, warp, L::kTmemCols)) return;
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 4) {
-    if (lane == 0) bwd_producer<D>(smem, bars, &tq, &tdo, q0, &tk, &tv, 0, n_iters, bh);
-    __syncwarp();
-  } else if (warp == 5) {
+  if (warp == kTmaWarp) {
+    bwd_producer<D>(smem, bars, &tq, &tdo, q0, &tk, &tv, 0, n_iters, bh, nullptr, nullptr, N);
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::kRes0);
       const uint32_t sdO = smem_u32(smem + L::kRes1);
-      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x211);
-      tc_fence_after_sync();
-      for (int n = 0; ok && n < n_iters; ++n) {
-        const int s = n % kStages;
-        const uint32_t sK = smem_u32(smem + L::kStr0 + s * L::kTileBytes);
-        const uint32_t sV = smem_u32(smem + L::kStr1 + s * L::kTileBytes);
-        if (!mbar_wait(&bars->str_full[s], (n / kStages) & 1, &bars->abort_flag, &g_bwd_error,
-                       0x212)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // S = Q_i K_j^T  and  dP = dO_i V_j^T
+      auto sK = [&](int n) { return smem_u32(smem + L::kStr0 + (n % kStages) * L::kTileBytes); };
+      auto sV = [&](int n) { return smem_u32(smem + L::kStr1 + (n % kStages) * L::kTileBytes); };
+      // S_n = Q K_n^T  and  dP_n = dO V_n^T
+      auto issue_s = [&](int n) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kSCol, kmajor_desc(sQ, kk), kmajor_desc(sK, kk), idesc_s,
-                  kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV, kk), idesc_s,
+          umma_ss(tmem + L::kSCol, kmajor_desc(sQ, kk), kmajor_desc(sK(n), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full);
-        // B += P K_j   (A = P bf16 in TMEM over S, B = K_j MN-major)
+      };
+      auto issue_dp = [&](int n) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV(n), kk), idesc_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->dp_full);
+      };
+      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x211) &&
+                mbar_wait(&bars->str_full[0], 0, &bars->abort_flag, &g_bwd_error, 0x212);
+      tc_fence_after_sync();
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      // order per step: B_n, S_{n+1}, dQ~_n, dP_{n+1}
+      for (int n = 0; ok && n < n_iters; ++n) {
+        // B += P K_n   (A = P bf16 in TMEM over S, B = K_n MN-major)
         if (!mbar_wait(&bars->p_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x214)) {
           ok = false;
           break;
@@ -478,9 +546,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kB, tmem + L::kSCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
-                  (n > 0 || kk > 0) ? 1u : 0u);
-        // dQ~ += dS~ K_j   (A = dS~ bf16 in TMEM over dP)
+          umma_ts(tmem + kB, tmem + L::kSCol + packed_a_col(kk), mnmajor_desc(sK(n), kk),
+                  idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+        const bool more = n + 1 < n_iters;
+        if (more) {
+          if (!mbar_wait(&bars->str_full[(n + 1) % kStages], ((n + 1) / kStages) & 1,
+                         &bars->abort_flag, &g_bwd_error, 0x215)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s(n + 1);
+        }
+        // dQ~ += dS~ K_n   (A = dS~ bf16 in TMEM over dP)
         if (!mbar_wait(&bars->ds_ready, n & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
           ok = false;
           break;
@@ -488,22 +566,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kDQ, tmem + L::kDPCol + kk * 8, mnmajor_desc(sK, kk), idesc_acc,
-                  (n > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->str_empty[s]);
+          umma_ts(tmem + kDQ, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sK(n), kk),
+                  idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->str_empty[n % kStages]);
+        if (more) issue_dp(n + 1);
       }
       if (ok) umma_commit(&bars->acc_done);
       umma_commit(&bars->drain);
     }
     __syncwarp();
   } else {
-    const int t = threadIdx.x;
+    const int T = threadIdx.x;
+    const int g = T >> 7;
+    const int t = T & 127;
     const int row = q0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t col0 = 64u * g;
     const bool rvalid = row < N;
     const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
     const float Dt = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;  // D~
-    float Dx = 0.0f;  // exact D = sum_j P_ij dP_ij
+    float Dx = 0.0f;  // this half's part of the exact D = sum_j P_ij dP_ij
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {
@@ -511,88 +593,97 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      uint32_t pr[128];
-      tmem_ld128(tmem + lane_off + L::kSCol, pr);
+      uint32_t pr[64];
+      tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
       const int kv0 = n * 128;
       const bool need_mask = (CAUSAL && n == n_iters - 1) || (kv0 + 128 > N);
       const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
       const int lim_n = N - 1 - kv0;
       const int lim = need_mask ? (lim_c < lim_n ? lim_c : lim_n) : 0x7fffffff;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
+      for (int c = 0; c < 64; ++c) {
         float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2));
-        if (c > lim) p = 0.0f;
+        if (static_cast<int>(col0) + c > lim) p = 0.0f;
         pr[c] = __float_as_uint(p);
       }
       {
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 32; ++c)
           pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
-        tmem_st32(tmem + lane_off + L::kSCol, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tmem + lane_off + L::kSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st32(tmem + lane_off + L::kSCol + col0, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars->p_ready);
+      if (!bwd_warp_wait(&bars->dp_full, n & 1, bars, 0x314)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kDPCol + c4 * 32, r);
+        tmem_ld32(tmem + lane_off + L::kDPCol + col0 + c2 * 32, r);
         tmem_ld_wait();
         reg_pin(r);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c = c4 * 32 + 2 * e;
+          const int c = c2 * 32 + 2 * e;
           const float p0 = __uint_as_float(pr[c]), p1 = __uint_as_float(pr[c + 1]);
           const float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
           Dx = fmaf(p0, dp0, Dx);
           Dx = fmaf(p1, dp1, Dx);
           w[e] = pack_bf16x2(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
         }
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-                tmem + lane_off + L::kDPCol + c4 * 16),
-            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
-            "r"(w[14]), "r"(w[15])
-            : "memory");
+        tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars->ds_ready);
     }
+    // combine the two halves' parts of D (bounded wait)
+    if (ok) {
+      dx_s[g * 128 + t] = Dx;
+      mbar_arrive(&bars->dx_ready);
+      ok = bwd_warp_wait(&bars->dx_ready, 0, bars, 0x313);
+    }
     if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x312)) {
       tc_fence_after_sync();
-      const float corr = Dx - Dt;
+      const float Dfull = dx_s[t] + dx_s[128 + t];
+      const float corr = Dfull - Dt;
       const size_t off = (static_cast<size_t>(bh) * N + (rvalid ? row : 0)) * D;
-      __nv_bfloat16* dst = dq + off;
+      // d = 128: warpgroup g stores dq columns [64g, 64g+64); d = 64: warpgroup 0 only
+      if (D == 128 || g == 0) {
+        const uint32_t c0 = (D == 128) ? col0 : 0u;
+        __nv_bfloat16* dst = dq + off + c0;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + kDQ + c * 32, a);
-        tmem_ld32(tmem + lane_off + kB + c * 32, b);
-        tmem_ld_wait();
-        reg_pin(a);
-        reg_pin(b);
-        uint32_t w[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t a[32], b[32];
+          tmem_ld32(tmem + lane_off + kDQ + c0 + c * 32, a);
+          tmem_ld32(tmem + lane_off + kB + c0 + c * 32, b);
+          tmem_ld_wait();
+          reg_pin(a);
+          reg_pin(b);
+          uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float x0 = scale * fmaf(-corr, __uint_as_float(b[2 * e]), __uint_as_float(a[2 * e]));
-          const float x1 =
-              scale * fmaf(-corr, __uint_as_float(b[2 * e + 1]), __uint_as_float(a[2 * e + 1]));
-          w[e] = pack_bf16x2(x0, x1);
-        }
-        if (rvalid) {
-          uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
+          for (int e = 0; e < 16; ++e) {
+            const float x0 =
+                scale * fmaf(-corr, __uint_as_float(b[2 * e]), __uint_as_float(a[2 * e]));
+            const float x1 =
+                scale * fmaf(-corr, __uint_as_float(b[2 * e + 1]), __uint_as_float(a[2 * e + 1]));
+            w[e] = pack_bf16x2(x0, x1);
+          }
+          if (rvalid) {
+            uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
-      if (rvalid) Dvec[static_cast<size_t>(bh) * N + row] = Dx;
+      if (g == 0 && rvalid) Dvec[static_cast<size_t>(bh) * N + row] = Dfull;
     }
   }
   bwd_teardown(bars, warp, tmem, L::kTmemCols);

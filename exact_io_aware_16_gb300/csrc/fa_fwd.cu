@@ -1,19 +1,22 @@
 // fa_fwd.cu — fused exact-attention forward for sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, head):
-//   * "What is Flash Attention?" 03:44-04:15 (tiling): the Q tile is loaded
-//     once and stays in shared memory while 128-row K and V tiles stream
-//     through a two-stage ring (TMA, 128-byte swizzle).
+// One CTA computes two 128-row query tiles (a "pair") of one (batch, head):
+//   * "What is Flash Attention?" 03:44-04:15 (tiling): both Q tiles are
+//     loaded once and stay in shared memory while 128-row K and V tiles
+//     stream through a two-stage ring (TMA, 128-byte swizzle); every K/V tile
+//     serves both Q tiles.
 //   * "Atencao exata ..." block-score formula S_ij = Q_i K_j^T / sqrt(d):
-//     tcgen05.mma writes the 128 x 128 fp32 score tile into tensor memory;
-//     two score buffers let S_{j+1} be computed while tile j's softmax runs.
-//   * transcript 04:46-05:17 (online softmax): each softmax thread owns one
-//     query row (= one TMEM lane), keeps the running max m (log2 units of the
-//     scaled scores) and running sum l, writes P~ = 2^(s*scale*log2e - m') as
-//     bf16 back over its score row, and rescales the O accumulator by
-//     alpha = 2^(m - m') when the max grows.  beta of the page is folded in
-//     by exponentiating against the new max directly (same arithmetic as the
-//     "l_new" formula of the mentria page).
+//     tcgen05.mma writes each 128 x 128 fp32 score tile into tensor memory.
+//   * transcript 04:46-05:17 (online softmax): one warpgroup per Q tile, one
+//     thread per query row (= one TMEM lane), keeps the running max m (log2
+//     units of the scaled scores) and running sum l, writes
+//     P~ = 2^(s*scale*log2e - m) as bf16 back over its score row, and
+//     rescales the O accumulator by alpha = 2^(m_old - m_new).  The running max
+//     is only moved when a row's block max exceeds it by more than 2^8
+//     (kLazyRescaleLog2): until then P~ <= 2^8 against the stale max, and since
+//     O and l are scaled by the same factor, O / l is unchanged.  beta of the
+//     page is folded in by exponentiating against the current max directly
+//     (the "l_new" formula of the mentria page).
 //   * O += P~ V_j is a tcgen05.mma with the P~ operand read from tensor
 //     memory and V from shared memory; O stays in tensor memory (fp32).
 //   * 06:52-07:24: at the end only O = O_acc / l (bf16) and one fp32
@@ -22,9 +25,15 @@
 //     tile i visits key tiles 0..i only; the mask is applied inside the
 //     diagonal tile, so whole tiles above the diagonal are never loaded.
 //
-// Warp roles (192 threads): warps 0-3 softmax / correction / epilogue (thread
-// t <-> query row t <-> TMEM lane t), warp 4 TMA producer, warp 5 TMEM
-// allocator and MMA issuer.
+// Ping-pong schedule of the MMA warp for key tile j:
+//     PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// so while warpgroup 0 turns S0 into P0 the tensor core runs PV1 and S1, and
+// the other way round.  Committing S_g(j+1) also guarantees that PV_g(j) has
+// completed, so a warpgroup that has seen its scores may rescale O at once.
+//
+// Warp roles (320 threads): warps 0-3 tile 0 and warps 4-7 tile 1
+// (softmax / correction / epilogue; thread t <-> row t <-> TMEM lane t),
+// warp 8 TMA producer, warp 9 TMEM allocator and MMA issuer.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,29 +47,32 @@ namespace {
 
 __device__ unsigned int g_fwd_error;
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLazyRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdLayout {
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;
+  static constexpr uint32_t kQ = 0;  // two Q tiles
+  static constexpr uint32_t kK = kQ + 2 * kTileBytes;
   static constexpr uint32_t kV = kK + kStages * kTileBytes;
   static constexpr uint32_t kBar = kV + kStages * kTileBytes;
   static constexpr uint32_t kSmem = kBar + 256 + 1024;  // + 1024-byte alignment slack
-  static constexpr uint32_t kTmemCols = 512;            // S0, S1, O
-  static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1
+  __host__ __device__ static constexpr uint32_t s_col(int g) { return 128u * g; }
+  __host__ __device__ static constexpr uint32_t o_col(int g) { return 256u + D * g; }
 };
 
 struct FwdBars {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_ready[2];
-  uint64_t pv_done;
+  uint64_t s_full[2], p_ready[2], pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -70,6 +82,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, FwdBar
                                           uint32_t code) {
   bool ok = mbar_wait(bar, parity, &b->abort_flag, &g_fwd_error, code);
   return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity, FwdBars* b,
+                                         uint32_t code) {
+  return mbar_wait(bar, parity, &b->abort_flag, &g_fwd_error, code);
 }
 
 template <int D, bool CAUSAL>
@@ -89,11 +106,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nq = (N + kTileM - 1) / kTileM;
-  // heaviest query tiles first across all heads
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int q0 = qt * kTileM;
-  const int nkv = CAUSAL ? (qt + 1) : (N + kTileN - 1) / kTileN;
+  const int nk = (N + kTileN - 1) / kTileN;
+  const int npairs = (nq + 1) / 2;
+  // head-major order (the query tiles of one head run together and share its
+  // K / V tiles in L2); within a head the heaviest (last) pair first
+  const int pair = npairs - 1 - static_cast<int>(blockIdx.x % npairs);
+  const int bh = static_cast<int>(blockIdx.x / npairs);
+  // key tiles visited by query tile 2*pair + g
+  const int nkv0 = CAUSAL ? min(2 * pair + 1, nk) : nk;
+  const int nkv1 = CAUSAL ? min(2 * pair + 2, nk) : nk;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -103,11 +124,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_ready[b], 128);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->p_ready[g], 128);
+      mbar_init(&bars->pv_done[g], 1);
     }
-    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->drain, 1);
     // an earlier CTA already recorded a pipeline timeout: exit without work
     bars->abort_flag = (*static_cast<volatile unsigned int*>(&g_fwd_error) != 0) ? 1 : 0;
@@ -115,7 +136,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   __syncthreads();
   if (bars->abort_flag) return;
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, L::kTmemCols);
     tmem_relinquish();
   }
@@ -124,17 +145,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&bars->q_full, L::kTileBytes);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTileBytes);
 #pragma unroll
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_load_3d(smem + L::kQ + c * 16384, &tq, &bars->q_full, c * 64, q0, bh);
-      for (int j = 0; j < nkv; ++j) {
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kQ + g * L::kTileBytes + c * 16384, &tq, &bars->q_full, c * 64,
+                      (2 * pair + g) * kTileM, bh);
+      for (int j = 0; j < nkv1; ++j) {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
         if (!mbar_wait(&bars->k_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x101)) break;
@@ -152,88 +176,103 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, &bars->abort_flag, &g_fwd_error, 0x201);
-      tc_fence_after_sync();
-      // O += P~_jp V_jp, P~ read from the score buffer of step jp
-      auto issue_pv = [&](int jp) -> bool {
-        const int bp = jp & 1;
-        const int sp = jp % kStages;
-        if (!mbar_wait(&bars->p_ready[bp], (jp >> 1) & 1, &bars->abort_flag, &g_fwd_error, 0x203))
-          return false;
-        if (!mbar_wait(&bars->v_full[sp], (jp / kStages) & 1, &bars->abort_flag, &g_fwd_error,
-                       0x204))
-          return false;
-        tc_fence_after_sync();
-        const uint32_t vbase = sV + sp * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, 16384, 1024);
-          umma_ts(tmem + L::kOCol, tmem + bp * 128 + kk * 8, bdesc, idesc_pv,
-                  (jp > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars->pv_done);
-        umma_commit(&bars->v_empty[sp]);
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % kStages;
-        const int b = j & 1;
-        if (!mbar_wait(&bars->k_full[s], (j / kStages) & 1, &bars->abort_flag, &g_fwd_error,
-                       0x202)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t kbase = sK + s * L::kTileBytes;
+      auto issue_s = [&](int g, int j) {
+        const uint32_t kbase = sK + (j % kStages) * L::kTileBytes;
+        const uint32_t qbase = sQ + g * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t adesc = sdesc_sw128(sQ + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(kbase + off, 16, 1024);
-          umma_ss(tmem + b * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + L::s_col(g), sdesc_sw128(qbase + off, 16, 1024),
+                  sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[b]);
-        umma_commit(&bars->k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        umma_commit(&bars->s_full[g]);
+      };
+      auto issue_pv = [&](int g, int j) {
+        const uint32_t vbase = sV + (j % kStages) * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          umma_ts(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
+                  sdesc_sw128(vbase + kk * 2048, 16384, 1024), idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->pv_done[g]);
+      };
+      bool ok = mma_wait(&bars->q_full, 0, bars, 0x201) &&
+                mma_wait(&bars->k_full[0], 0, bars, 0x202);
+      tc_fence_after_sync();
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(&bars->k_empty[0]);
       }
-      if (ok) issue_pv(nkv - 1);
+      for (int j = 0; ok && j < nkv1; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        const int sn = (j + 1) % kStages;
+        const uint32_t phn = ((j + 1) / kStages) & 1;
+        bool v_ready = false, k_next_ready = false;
+        if (j < nkv0) {
+          ok = mma_wait(&bars->p_ready[0], j & 1, bars, 0x203) &&
+               mma_wait(&bars->v_full[s], ph, bars, 0x204);
+          if (!ok) break;
+          v_ready = true;
+          tc_fence_after_sync();
+          issue_pv(0, j);
+          if (j + 1 < nkv0) {
+            if (!mma_wait(&bars->k_full[sn], phn, bars, 0x205)) { ok = false; break; }
+            k_next_ready = true;
+            tc_fence_after_sync();
+            issue_s(0, j + 1);
+          }
+        }
+        ok = mma_wait(&bars->p_ready[1], j & 1, bars, 0x206) &&
+             (v_ready || mma_wait(&bars->v_full[s], ph, bars, 0x207));
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv(1, j);
+        umma_commit(&bars->v_empty[s]);
+        if (j + 1 < nkv1) {
+          if (!k_next_ready && !mma_wait(&bars->k_full[sn], phn, bars, 0x208)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s(1, j + 1);
+          umma_commit(&bars->k_empty[sn]);
+        }
+      }
       umma_commit(&bars->drain);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ softmax warps 0-3
-    const int t = threadIdx.x;  // query row within the tile, TMEM lane
-    const int row = q0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    float m_run = -INFINITY;  // running max of s * scale * log2(e)
+    // ------------------------------------------------ softmax warpgroups
+    const int g = warp >> 2;           // which query tile of the pair
+    const int t = threadIdx.x & 127;   // row within the tile, TMEM lane
+    const int row = (2 * pair + g) * kTileM + t;
+    const int nkv = g ? nkv1 : nkv0;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t scol = tmem + lane_off + L::s_col(g);
+    const uint32_t ocol = tmem + lane_off + L::o_col(g);
+    float m_run = -INFINITY;  // running (lazily moved) max of s * scale * log2(e)
     float l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int b = j & 1;
-      if (!warp_wait(&bars->s_full[b], (j >> 1) & 1, bars, 0x301)) {
+      if (!warp_wait(&bars->s_full[g], j & 1, bars, 0x301)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       uint32_t sr[128];
-      {
-        uint32_t(&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t(&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        uint32_t(&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-        uint32_t(&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-        const uint32_t base = tmem + lane_off + b * 128;
-        tmem_ld32(base + 0, c0);
-        tmem_ld32(base + 32, c1);
-        tmem_ld32(base + 64, c2);
-        tmem_ld32(base + 96, c3);
-        tmem_ld_wait();
-        reg_pin(sr);
-      }
+      tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      tmem_ld_wait();
+      reg_pin(sr);
       const int kv0 = j * kTileN;
       const bool need_mask = (CAUSAL && j == nkv - 1) || (kv0 + kTileN > N);
       if (need_mask) {
@@ -247,59 +286,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float mx = __uint_as_float(sr[0]);
 #pragma unroll
       for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      const float m_new = fmaxf(m_run, mx * scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+      const float m_blk = mx * scale_log2;
+      // move the running max only when some row of the warp needs it
+      const bool move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
+      float alpha = 1.0f;
+      if (move) {
+        const float m_new = fmaxf(m_run, m_blk);
+        alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       float sum = 0.0f;
-      uint32_t pk[64];
+      // P~ packed in place: pair c overwrites sr[c], already consumed
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
         sum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        sr[c] = pack_bf16x2(p0, p1);
       }
-      {
-        const uint32_t base = tmem + lane_off + b * 128;
-        tmem_st32(base + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      }
-      const float alpha = ex2_approx(m_run - m_use);  // 0 on the first tile
-      l_run = l_run * alpha + sum;
-      m_run = m_new;
-      if (j > 0) {
-        // O holds P~_{j-1} V_{j-1} only once that MMA has completed
-        if (!warp_wait(&bars->pv_done, (j - 1) & 1, bars, 0x302)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      if (move && j > 0) {
+        // PV_g(j-1) completed before S_g(j) was reported, and PV_g(j) is not
+        // issued before p_ready: O is stable here
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(ocol + c * 32, r);
+          tmem_ld_wait();
+          reg_pin(r);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            const uint32_t addr = tmem + lane_off + L::kOCol + c * 32;
-            tmem_ld32(addr, r);
-            tmem_ld_wait();
-            reg_pin(r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(addr, r);
-          }
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(ocol + c * 32, r);
         }
       }
+      l_run += sum;
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->p_ready[b]);
+      mbar_arrive(&bars->p_ready[g]);
     }
     // ------------------------------------------------ epilogue
-    if (ok && warp_wait(&bars->pv_done, (nkv - 1) & 1, bars, 0x303)) {
+    if (ok && warp_wait(&bars->pv_done[g], (nkv - 1) & 1, bars, 0x303)) {
       tc_fence_after_sync();
       const float inv_l = 1.0f / l_run;
       __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kOCol + c * 32, r);
+        tmem_ld32(ocol + c * 32, r);
         tmem_ld_wait();
         reg_pin(r);
         uint32_t w[16];
@@ -318,7 +354,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 
   // ------------------------------------------------ teardown
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     // every MMA this CTA issued has completed before TMEM is released
     mbar_wait(&bars->drain, 0, &bars->abort_flag, &g_fwd_error, 0x205);
   }
@@ -330,7 +366,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -343,7 +379,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long nq = (a.N + kTileM - 1) / kTileM;
-  const long long blocks = nq * a.BH;
+  const long long blocks = (nq + 1) / 2 * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2);
