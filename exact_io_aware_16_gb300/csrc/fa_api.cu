@@ -60,16 +60,15 @@ int check_arch() {
   return ok ? FA_OK : FA_ERR_ARCH;
 }
 
-// [BH][N][d] bf16 as a 3-D tensor (d, N, BH); box 64 x 128 x 1, 128B swizzle.
-int encode_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d) {
+// [BH][N][d] bf16 as a 3-D tensor (d, N, BH); box 64 x rows x 1, 128B swizzle.
+int encode_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int rows) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return FA_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols), static_cast<cuuint32_t>(fa::kTileM),
-                       1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols), static_cast<cuuint32_t>(rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -118,8 +117,9 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((st = check_arch()) != FA_OK) return st;
   const int BH = B * H;
   fa::TensorMaps maps;
-  if (encode_bhnd(&maps.q, q, BH, N, d) != FA_OK || encode_bhnd(&maps.k, k, BH, N, d) != FA_OK ||
-      encode_bhnd(&maps.v, v, BH, N, d) != FA_OK)
+  if (encode_bhnd(&maps.q, q, BH, N, d, 128) != FA_OK ||
+      encode_bhnd(&maps.k, k, BH, N, d, 128) != FA_OK ||
+      encode_bhnd(&maps.v, v, BH, N, d, 128) != FA_OK)
     return FA_ERR_CUDA;
   fa::FwdArgs a;
   a.tq = &maps.q;
@@ -168,8 +168,10 @@ static int bwd_step(const void* q, const void* k, const void* v, const void* dO,
   if ((st = check_arch()) != FA_OK) return st;
   const int BH = B * H;
   fa::TensorMaps maps;
-  if (encode_bhnd(&maps.q, q, BH, N, d) != FA_OK || encode_bhnd(&maps.k, k, BH, N, d) != FA_OK ||
-      encode_bhnd(&maps.v, v, BH, N, d) != FA_OK || encode_bhnd(&maps.dO, dO, BH, N, d) != FA_OK)
+  if (encode_bhnd(&maps.q, q, BH, N, d, 128) != FA_OK ||
+      encode_bhnd(&maps.k, k, BH, N, d, 128) != FA_OK ||
+      encode_bhnd(&maps.v, v, BH, N, d, 128) != FA_OK ||
+      encode_bhnd(&maps.dO, dO, BH, N, d, 128) != FA_OK)
     return FA_ERR_CUDA;
   fa::BwdArgs a;
   a.tq = &maps.q;

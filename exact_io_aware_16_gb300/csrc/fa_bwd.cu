@@ -406,12 +406,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pr[64];
       tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
       const bool diag = CAUSAL && (it == kt);
+      const float4* lse4 = reinterpret_cast<const float4*>(lse2_s + col0);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int qc = col0 + c;
-        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2_s[qc]));
-        if (diag && (q0 + qc < krow)) p = 0.0f;  // query before key: masked
-        pr[c] = __float_as_uint(p);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = lse4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lv[e]));
+          if (diag && (q0 + static_cast<int>(col0) + c < krow)) p = 0.0f;  // query before key
+          pr[c] = __float_as_uint(p);
+        }
       }
       {
         uint32_t pk[32];
@@ -436,13 +442,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait();
         reg_pin(r);
         uint32_t w[16];
+        const float4* d4 = reinterpret_cast<const float4*>(D_s + col0 + c2 * 32);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = c2 * 32 + 2 * e;
-          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[2 * e]) - D_s[col0 + c]);
-          const float ds1 =
-              __uint_as_float(pr[c + 1]) * (__uint_as_float(r[2 * e + 1]) - D_s[col0 + c + 1]);
-          w[e] = pack_bf16x2(ds0, ds1);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 dd = d4[e4];
+          const int c = c2 * 32 + 4 * e4;
+          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[4 * e4]) - dd.x);
+          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[4 * e4 + 1]) - dd.y);
+          const float ds2 = __uint_as_float(pr[c + 2]) * (__uint_as_float(r[4 * e4 + 2]) - dd.z);
+          const float ds3 = __uint_as_float(pr[c + 3]) * (__uint_as_float(r[4 * e4 + 3]) - dd.w);
+          w[2 * e4] = pack_bf16x2(ds0, ds1);
+          w[2 * e4 + 1] = pack_bf16x2(ds2, ds3);
         }
         tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
       }
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool rvalid = row < N;
     const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
     const float Dt = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;  // D~
-    float Dx = 0.0f;  // this half's part of the exact D = sum_j P_ij dP_ij
+    float dxp[4] = {0.f, 0.f, 0.f, 0.f};  // this half's part of the exact D = sum_j P_ij dP_ij
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {
@@ -633,8 +643,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int c = c2 * 32 + 2 * e;
           const float p0 = __uint_as_float(pr[c]), p1 = __uint_as_float(pr[c + 1]);
           const float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
-          Dx = fmaf(p0, dp0, Dx);
-          Dx = fmaf(p1, dp1, Dx);
+          dxp[(2 * e) & 3] = fmaf(p0, dp0, dxp[(2 * e) & 3]);
+          dxp[(2 * e + 1) & 3] = fmaf(p1, dp1, dxp[(2 * e + 1) & 3]);
           w[e] = pack_bf16x2(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
         }
         tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
@@ -645,7 +655,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // combine the two halves' parts of D (bounded wait)
     if (ok) {
-      dx_s[g * 128 + t] = Dx;
+      dx_s[g * 128 + t] = (dxp[0] + dxp[1]) + (dxp[2] + dxp[3]);
       mbar_arrive(&bars->dx_ready);
       ok = bwd_warp_wait(&bars->dx_ready, 0, bars, 0x313);
     }

@@ -13,9 +13,11 @@ constexpr int kTileN = 128;   // key rows per tile
 constexpr int kBoxCols = 64;  // bf16 columns per 128-byte swizzled TMA box
 
 // A [BH][N][d] bf16 tensor seen by TMA as a 3-D tensor (d, N, BH) with
-// 64 x 128 x 1 boxes and 128-byte swizzle.  Rows past N read as zero.
+// 64-column boxes of 128 rows (resident tiles) or 64 rows (streamed tiles) and
+// 128-byte swizzle.  Rows past N read as zero.
 struct TensorMaps {
-  CUtensorMap q, k, v, o, dO;
+  CUtensorMap q, k, v, dO;          // 128-row boxes
+  CUtensorMap q64, k64, v64, dO64;  // 64-row boxes
 };
 
 struct FwdArgs {
