@@ -299,7 +299,10 @@ def run_ours(args, world, rank, local):
 
     # dominant kernel and its roofline (algorithmic work of that kernel alone)
     base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
-    kflops = {"fwd": 4 * base, "bwd_dkdv": 8 * base, "bwd_dq": 2 * base, "bwd_pre": 0.0}
+    # per-kernel algorithmic FLOPs: the matmuls that kernel's own outputs require
+    # (dQ needs S, dP and dS K; dK/dV need S, dP, P^T dO and dS^T Q), so the
+    # recomputed S and dP count in both backward kernels
+    kflops = {"fwd": 4 * base, "bwd_dkdv": 8 * base, "bwd_dq": 6 * base, "bwd_pre": 0.0}
     tbytes = w.B * w.H * w.N * w.d * 2
     kbytes = {"bwd_pre": 2 * tbytes + w.B * w.H * w.N * 4}
     dom = max(names, key=lambda n: per_kernel[n])
