@@ -20,6 +20,9 @@ What each function follows:
   06:52-07:24 and 08:26).
 * ``online_softmax`` / ``online_attention_row``: the running-max update of
   transcript 04:46-05:17, used only to pin online == two-pass.
+* ``mask=`` (block-sparse, the talk's block-sparse FlashAttention): scores of
+  dropped (query block, key block) pairs are -inf; a row with no visible key
+  is defined as o = 0, lse = -inf with zero gradients.
 
 Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
 """
@@ -116,6 +119,8 @@ class Oracle:
                                                 ip, i64, dp, dp, i]
         lib.fa_oracle_online_softmax.argtypes = [dp, i, i, dp, dp]
         lib.fa_oracle_online_attention_row.argtypes = [dp, dp, i, i, i, dp, dp]
+        lib.fa_oracle_set_block_mask.argtypes = [ctypes.c_void_p, i, i, i, i64]
+        lib.fa_oracle_set_block_mask.restype = None
         for f in (lib.fa_oracle_forward, lib.fa_oracle_backward_rows,
                   lib.fa_oracle_backward_cols, lib.fa_oracle_online_softmax,
                   lib.fa_oracle_online_attention_row):
@@ -123,8 +128,37 @@ class Oracle:
         self.lib = lib
         self.path = lib_path
 
+    def _masked(self, mask, block, BH):
+        """Context manager that installs a block mask for the calls inside it.
+
+        mask: uint8 array [nqb, nkb] (shared by every (b,h)) or [BH, nqb, nkb];
+        nonzero keeps the (query block, key block) pair.  block = (bq, bk) rows.
+        """
+        lib = self.lib
+
+        class _Ctx:
+            def __enter__(ctx):
+                if mask is None:
+                    return ctx
+                m = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+                if m.ndim == 2:
+                    m = m[None]
+                if m.shape[0] not in (1, BH):
+                    raise ValueError("mask must be [nqb, nkb] or [BH, nqb, nkb]")
+                ctx.m = m
+                stride = 0 if m.shape[0] == 1 else m.shape[1] * m.shape[2]
+                lib.fa_oracle_set_block_mask(m.ctypes.data, int(block[0]), int(block[1]),
+                                             int(m.shape[2]), int(stride))
+                return ctx
+
+            def __exit__(ctx, *exc):
+                lib.fa_oracle_set_block_mask(None, 1, 1, 0, 0)
+                return False
+
+        return _Ctx()
+
     def forward(self, q, k, v, scale: float, causal: bool, rows=None,
-                nthreads: int | None = None):
+                nthreads: int | None = None, mask=None, block=(128, 128)):
         """O and lse of the definition.
 
         q, k, v: [B,H,N,d] or [BH,N,d] (any dtype; converted exactly to float64).
@@ -136,15 +170,16 @@ class Oracle:
         sel, n = _sel(rows, BH, N)
         o = np.empty((n, d), np.float64)
         lse = np.empty((n,), np.float64)
-        rc = self.lib.fa_oracle_forward(
-            _ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n,
-            _ptr(o), _ptr(lse), int(nthreads or default_threads()))
+        with self._masked(mask, block, BH):
+            rc = self.lib.fa_oracle_forward(
+                _ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale), int(bool(causal)),
+                _iptr(sel), n, _ptr(o), _ptr(lse), int(nthreads or default_threads()))
         if rc != 0:
             raise RuntimeError(f"fa_oracle_forward failed ({rc})")
         return o, lse
 
     def backward_rows(self, q, k, v, dO, scale: float, causal: bool, rows=None,
-                      nthreads: int | None = None):
+                      nthreads: int | None = None, mask=None, block=(128, 128)):
         """Row pass: dq for the selected rows plus per-row m, l, D and D_alt.
 
         D is sum_j P_ij dP_ij; D_alt is sum_c dO_ic O_ic.  They agree exactly in
@@ -158,16 +193,17 @@ class Oracle:
         l = np.empty((n,), np.float64)
         D = np.empty((n,), np.float64)
         D_alt = np.empty((n,), np.float64)
-        rc = self.lib.fa_oracle_backward_rows(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(dO), BH, N, d, float(scale), int(bool(causal)),
-            _iptr(sel), n, _ptr(dq), _ptr(m), _ptr(l), _ptr(D), _ptr(D_alt),
-            int(nthreads or default_threads()))
+        with self._masked(mask, block, BH):
+            rc = self.lib.fa_oracle_backward_rows(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(dO), BH, N, d, float(scale), int(bool(causal)),
+                _iptr(sel), n, _ptr(dq), _ptr(m), _ptr(l), _ptr(D), _ptr(D_alt),
+                int(nthreads or default_threads()))
         if rc != 0:
             raise RuntimeError(f"fa_oracle_backward_rows failed ({rc})")
         return dq, m, l, D, D_alt
 
     def backward_cols(self, q, k, v, dO, m_all, l_all, D_all, scale: float, causal: bool,
-                      cols=None, nthreads: int | None = None):
+                      cols=None, nthreads: int | None = None, mask=None, block=(128, 128)):
         """Column pass: dk, dv for the selected key rows (flat bh*N + j).
 
         m_all, l_all, D_all must cover every row (from backward_rows(rows=None)).
@@ -180,18 +216,22 @@ class Oracle:
         sel, n = _sel(cols, BH, N)
         dk = np.empty((n, d), np.float64)
         dv = np.empty((n, d), np.float64)
-        rc = self.lib.fa_oracle_backward_cols(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(m_all), _ptr(l_all), _ptr(D_all),
-            BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n, _ptr(dk), _ptr(dv),
-            int(nthreads or default_threads()))
+        with self._masked(mask, block, BH):
+            rc = self.lib.fa_oracle_backward_cols(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(m_all), _ptr(l_all), _ptr(D_all),
+                BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n, _ptr(dk), _ptr(dv),
+                int(nthreads or default_threads()))
         if rc != 0:
             raise RuntimeError(f"fa_oracle_backward_cols failed ({rc})")
         return dk, dv
 
-    def backward(self, q, k, v, dO, scale: float, causal: bool, nthreads: int | None = None):
+    def backward(self, q, k, v, dO, scale: float, causal: bool, nthreads: int | None = None,
+                 mask=None, block=(128, 128)):
         """Full backward: (dq, dk, dv) each [BH*N, d], plus (m, l, D, D_alt) per row."""
-        dq, m, l, D, D_alt = self.backward_rows(q, k, v, dO, scale, causal, None, nthreads)
-        dk, dv = self.backward_cols(q, k, v, dO, m, l, D, scale, causal, None, nthreads)
+        dq, m, l, D, D_alt = self.backward_rows(q, k, v, dO, scale, causal, None, nthreads,
+                                                mask=mask, block=block)
+        dk, dv = self.backward_cols(q, k, v, dO, m, l, D, scale, causal, None, nthreads,
+                                    mask=mask, block=block)
         return dq, dk, dv, (m, l, D, D_alt)
 
     def online_softmax(self, x, block: int):

@@ -31,6 +31,12 @@
  *    aligned); masked scores are -inf before the softmax.
  *  - the stored statistic is lse_i = m_i + ln l_i (natural log of the scaled
  *    scores), which is the pair (m, l) folded into one number.
+ *  - block-sparse masks ("FlashAttention: fast and memory-efficient exact
+ *    attention with IO-awareness" talk, block-sparse FlashAttention): an
+ *    optional block mask marks whole (query block, key block) pairs as
+ *    skipped; their scores are -inf, which is exact attention restricted to
+ *    the kept blocks.  A row with no visible key has no softmax; it is defined
+ *    here as o = 0, lse = -inf and zero gradients.
  *
  * Layout: every [BH][N][d] array is row-major with index (bh*N + i)*d + c.
  * Row / column selections are flat indices r = bh*N + i.
@@ -109,6 +115,10 @@ typedef struct {
   int BH, N, d, causal;
   double scale;
   const int64_t* sel; /* selected flat rows / columns, or NULL = all */
+  /* optional block mask: visible iff bmask[bh*mstride + (i/bq)*nkb + j/bk] */
+  const uint8_t* bmask;
+  int bq, bk, nkb;
+  int64_t mstride;
   /* forward outputs */
   double *o, *lse;
   /* backward-row outputs */
@@ -118,9 +128,12 @@ typedef struct {
   double *dk, *dv;
 } job_t;
 
-/* s_ij = scale * sum_c q_ic k_jc, or -inf when causal and j > i. */
+/* s_ij = scale * sum_c q_ic k_jc, or -inf when causal and j > i, or when the
+ * block mask drops the (i, j) block. */
 static double score(const job_t* J, int64_t bh, int i, int j) {
   if (J->causal && j > i) return -INFINITY;
+  if (J->bmask && !J->bmask[bh * J->mstride + (int64_t)(i / J->bq) * J->nkb + j / J->bk])
+    return -INFINITY;
   const double* qi = J->q + ((size_t)bh * J->N + i) * J->d;
   const double* kj = J->k + ((size_t)bh * J->N + j) * J->d;
   double acc = 0.0;
@@ -137,6 +150,12 @@ static void softmax_row(const job_t* J, int64_t bh, int i, double* s, double* p,
   for (int j = 0; j < N; ++j) {
     s[j] = score(J, bh, i, j);
     if (s[j] > m) m = s[j];
+  }
+  if (m == -INFINITY) { /* no visible key: p = 0, l = 0 */
+    for (int j = 0; j < N; ++j) p[j] = 0.0;
+    *m_ret = m;
+    *l_ret = 0.0;
+    return;
   }
   double l = 0.0;
   for (int j = 0; j < N; ++j) l += exp(s[j] - m); /* e^{-inf} = 0 */
@@ -161,7 +180,33 @@ static void fwd_item(void* ctx, int64_t it, double* scratch) {
       acc += p[j] * J->v[((size_t)bh * J->N + j) * J->d + c];
     oi[c] = acc;
   }
-  J->lse[it] = m + log(l);
+  J->lse[it] = (l > 0.0) ? m + log(l) : -INFINITY;
+}
+
+static void set_mask(job_t* J, const uint8_t* bmask, int bq, int bk, int nkb, int64_t mstride) {
+  J->bmask = bmask;
+  J->bq = bq > 0 ? bq : 1;
+  J->bk = bk > 0 ? bk : 1;
+  J->nkb = nkb;
+  J->mstride = mstride;
+}
+
+/* the masked entry points below take the block mask as set by the caller
+ * through this thread-local pointer, so the unmasked signatures stay as they
+ * are */
+static __thread const uint8_t* t_bmask = 0;
+static __thread int t_bq = 1, t_bk = 1, t_nkb = 0;
+static __thread int64_t t_mstride = 0;
+
+/* Set (or clear with bmask = NULL) the block mask for the next calls made by
+ * this thread: bmask[bh * mstride + qb * nkb + kb] != 0 keeps the block of
+ * query rows [qb*bq, qb*bq+bq) and key rows [kb*bk, kb*bk+bk). */
+void fa_oracle_set_block_mask(const uint8_t* bmask, int bq, int bk, int nkb, int64_t mstride) {
+  t_bmask = bmask;
+  t_bq = bq;
+  t_bk = bk;
+  t_nkb = nkb;
+  t_mstride = mstride;
 }
 
 /* O = P V and lse = m + ln l for the selected rows (all rows when sel is
@@ -175,6 +220,7 @@ int fa_oracle_forward(const double* q, const double* k, const double* v, int BH,
   J.q = q; J.k = k; J.v = v;
   J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
   J.sel = sel; J.o = o; J.lse = lse;
+  set_mask(&J, t_bmask, t_bq, t_bk, t_nkb, t_mstride);
   if (!sel) n_rows = (int64_t)BH * N;
   return run_pool(fwd_item, &J, n_rows, (size_t)2 * N, nthreads);
 }
@@ -237,6 +283,7 @@ int fa_oracle_backward_rows(const double* q, const double* k, const double* v, c
   J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
   J.sel = sel; J.dq = dq; J.m_out = m_out; J.l_out = l_out;
   J.D_out = D_out; J.D_alt_out = D_alt_out;
+  set_mask(&J, t_bmask, t_bq, t_bk, t_nkb, t_mstride);
   if (!sel) n_rows = (int64_t)BH * N;
   return run_pool(bwd_row_item, &J, n_rows, (size_t)3 * N, nthreads);
 }
@@ -286,6 +333,7 @@ int fa_oracle_backward_cols(const double* q, const double* k, const double* v, c
   J.BH = BH; J.N = N; J.d = d; J.causal = causal; J.scale = scale;
   J.sel = sel; J.m_all = m_all; J.l_all = l_all; J.D_all = D_all;
   J.dk = dk; J.dv = dv;
+  set_mask(&J, t_bmask, t_bq, t_bk, t_nkb, t_mstride);
   if (!sel) n_cols = (int64_t)BH * N;
   return run_pool(bwd_col_item, &J, n_cols, 1, nthreads);
 }

@@ -330,6 +330,82 @@ def pin_selection_consistency(orc):
         assert np.array_equal(dks, dk[rows]) and np.array_equal(dvs, dv[rows])
 
 
+# ---------------------------------------------------------------- pin 10
+def _expand(mask, bq, bk, N):
+    """Element mask [.., N, N] from a block mask [.., nqb, nkb]."""
+    m = np.asarray(mask, dtype=bool)
+    return np.repeat(np.repeat(m, bq, axis=-2), bk, axis=-1)[..., :N, :N]
+
+
+def pin_block_mask(orc):
+    """Block-sparse masking (the talk's block-sparse FlashAttention):
+    * an all-ones block mask changes nothing (bit for bit);
+    * a block-diagonal mask splits the problem into independent dense
+      attention problems, one per block (O, lse and all three gradients);
+    * against PyTorch's fp64 SDPA with the element-expanded boolean mask,
+      with uneven block sizes (bq != bk), per-head masks and causal on top;
+    * rows whose blocks are all dropped give o = 0, lse = -inf and zero dq,
+      and do not change dk, dv of other rows."""
+    rng = _rng(10)
+    BH, N, d, scale = 2, 22, 8, 0.4
+    q, k, v, dO = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    ones = np.ones((6, 8), np.uint8)  # bq=4, bk=3
+    a = orc.forward(q, k, v, scale, True)
+    b = orc.forward(q, k, v, scale, True, mask=ones, block=(4, 3))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # block diagonal with square blocks of 5 rows: independent sub-problems
+    nb = -(-N // 5)
+    diag = np.eye(nb, dtype=np.uint8)
+    o, lse = orc.forward(q, k, v, scale, False, mask=diag, block=(5, 5))
+    dq, dk, dv, _ = orc.backward(q, k, v, dO, scale, False, mask=diag, block=(5, 5))
+    o, lse, dq, dk, dv = (x.reshape(BH, N, *x.shape[1:]) for x in (o, lse, dq, dk, dv))
+    for b0 in range(0, N, 5):
+        sl = slice(b0, min(b0 + 5, N))
+        ob, lb = orc.forward(q[:, sl], k[:, sl], v[:, sl], scale, False)
+        gq, gk, gv, _ = orc.backward(q[:, sl], k[:, sl], v[:, sl], dO[:, sl], scale, False)
+        n = sl.stop - sl.start
+        _close(o[:, sl].reshape(-1, d), ob, 1e-13, atol=1e-15, what="block-diag O")
+        _close(lse[:, sl].reshape(-1), lb, 1e-13, atol=1e-15, what="block-diag lse")
+        for got, ref, nm in ((dq, gq, "dQ"), (dk, gk, "dK"), (dv, gv, "dV")):
+            _close(got[:, sl].reshape(-1, d), ref.reshape(BH * n, d), 1e-12, atol=1e-14,
+                   what=f"block-diag {nm}")
+    # random per-head masks, uneven blocks, against torch SDPA (every row keeps a block)
+    bq, bk = 4, 3
+    nqb, nkb = -(-N // bq), -(-N // bk)
+    for causal in (False, True):
+        mask = (rng.random((BH, nqb, nkb)) < 0.5).astype(np.uint8)
+        mask[:, :, 0] = 1  # key block 0 is visible to every row (also under causal)
+        el = _expand(mask, bq, bk, N)
+        if causal:
+            el = el & np.tril(np.ones((N, N), dtype=bool))
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, attn_mask=torch.tensor(el), scale=scale)
+        to.backward(torch.tensor(dO))
+        s_ = (tq @ tk.transpose(-1, -2)).detach() * scale
+        tlse = torch.logsumexp(s_.masked_fill(~torch.tensor(el), -math.inf), dim=-1)
+        o, lse = orc.forward(q, k, v, scale, causal, mask=mask, block=(bq, bk))
+        dq, dk, dv, _ = orc.backward(q, k, v, dO, scale, causal, mask=mask, block=(bq, bk))
+        _close(o, to.detach().reshape(-1, d).numpy(), 1e-10, atol=1e-12, what="masked O vs sdpa")
+        _close(lse, tlse.reshape(-1).numpy(), 1e-12, atol=1e-13, what="masked lse vs sdpa")
+        for got, t, nm in ((dq, tq, "dQ"), (dk, tk, "dK"), (dv, tv, "dV")):
+            _close(got, t.grad.reshape(-1, d).numpy(), 1e-9, atol=1e-11, what=f"masked {nm}")
+    # fully dropped query block 1 (rows 4..7): o = 0, lse = -inf, dq = 0
+    mask = np.ones((nqb, nkb), np.uint8)
+    mask[1, :] = 0
+    o, lse = orc.forward(q, k, v, scale, False, mask=mask, block=(bq, bk))
+    dq, dk, dv, _ = orc.backward(q, k, v, dO, scale, False, mask=mask, block=(bq, bk))
+    o, lse, dq = o.reshape(BH, N, d), lse.reshape(BH, N), dq.reshape(BH, N, d)
+    assert np.all(o[:, 4:8] == 0.0) and np.all(lse[:, 4:8] == -np.inf) and np.all(dq[:, 4:8] == 0)
+    # a dropped row contributes nothing to dK, dV: same as the unmasked problem
+    # with that row's upstream gradient set to zero
+    dO0 = dO.copy()
+    dO0[:, 4:8] = 0.0
+    g = orc.backward(q, k, v, dO0, scale, False)
+    _close(dk, g[1], 1e-12, atol=1e-14, what="dK without the dropped rows")
+    _close(dv, g[2], 1e-12, atol=1e-14, what="dV without the dropped rows")
+
+
 ALL_PINS = [pin_worked_example, pin_zero_query, pin_one_hot, pin_permutation,
             pin_online_equals_two_pass, pin_finite_differences, pin_structure,
-            pin_torch_sdpa, pin_selection_consistency]
+            pin_torch_sdpa, pin_selection_consistency, pin_block_mask]

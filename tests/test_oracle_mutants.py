@@ -18,7 +18,8 @@ MUTANTS = [
      "if (J->causal && j > i + 1) return -INFINITY;"),
     ("dP_uses_k", "const double* vj = J->v + ((size_t)bh * N + j) * d;\n    double acc = 0.0;",
      "const double* vj = J->k + ((size_t)bh * N + j) * d;\n    double acc = 0.0;"),
-    ("lse_log2", "J->lse[it] = m + log(l);", "J->lse[it] = m + log2(l);"),
+    ("lse_log2", "J->lse[it] = (l > 0.0) ? m + log(l) : -INFINITY;",
+     "J->lse[it] = (l > 0.0) ? m + log2(l) : -INFINITY;"),
     ("online_beta_dropped", "l = alpha * l + beta * blk_sum;\n    m = m_new;\n    if (m_trace)",
      "l = alpha * l + blk_sum;\n    m = m_new;\n    if (m_trace)"),
     ("dv_uses_dS", "dvj[c] += p * dOi[c];", "dvj[c] += dS * dOi[c];"),
@@ -32,6 +33,10 @@ MUTANTS = [
     ("col_pass_D_dropped", "const double dS = p * (dP - J->D_all[ri]);",
      "const double dS = p * dP;"),
     ("online_O_alpha_dropped", "for (int c = 0; c < d; ++c) o[c] *= alpha;", "(void)0;"),
+    ("block_mask_ignored", "if (J->bmask && !J->bmask[", "if (0 && !J->bmask["),
+    ("block_mask_axes_swapped", "(int64_t)(i / J->bq) * J->nkb + j / J->bk]",
+     "(int64_t)(j / J->bq) * J->nkb + i / J->bk]"),
+    ("block_mask_ignores_head", "J->bmask[bh * J->mstride +", "J->bmask[0 * J->mstride +"),
 ]
 
 
