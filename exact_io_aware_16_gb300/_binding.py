@@ -54,6 +54,12 @@ def library():
         lib.fa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz,
                                     vp]
         lib.fa_backward.restype = i
+        ll = ctypes.c_longlong
+        lib.fa_forward_blocksparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ll, vp]
+        lib.fa_forward_blocksparse.restype = i
+        lib.fa_backward_blocksparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
+                                                i, vp, ll, vp, sz, vp]
+        lib.fa_backward_blocksparse.restype = i
         lib.fa_backward_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.fa_backward_preprocess.restype = i
         lib.fa_backward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i,
@@ -122,6 +128,62 @@ def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, o=None
     if st != FA_OK:
         raise FaError(st, "fa_forward")
     return o, lse
+
+
+def _mask_args(mask, B, H, N):
+    """(pointer, head stride) of a uint8 CUDA block mask [nt,nt] or [B*H,nt,nt]."""
+    nt = -(-N // 128)
+    if mask.dtype != torch.uint8 or not mask.is_cuda or not mask.is_contiguous():
+        raise TypeError("block mask must be a contiguous uint8 CUDA tensor")
+    if tuple(mask.shape) == (nt, nt):
+        return ctypes.c_void_p(mask.data_ptr()), 0
+    if tuple(mask.shape) == (B * H, nt, nt):
+        return ctypes.c_void_p(mask.data_ptr()), nt * nt
+    raise ValueError(f"block mask must be [{nt},{nt}] or [{B * H},{nt},{nt}]")
+
+
+def fa_forward_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None,
+                           o=None, lse=None, stream=None):
+    """fa_forward restricted to the 128x128 tiles a uint8 block mask keeps."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    mp, ms = _mask_args(block_mask, B, H, N)
+    st = library().fa_forward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
+                                          d, float(scale), int(bool(causal)), mp, ms,
+                                          ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward_blocksparse")
+    return o, lse
+
+
+def fa_backward_blocksparse(q, k, v, o, dO, lse, block_mask, causal: bool = False,
+                            scale: float | None = None, dq=None, dk=None, dv=None,
+                            workspace=None, stream=None):
+    """fa_backward restricted to the 128x128 tiles a uint8 block mask keeps."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_backward_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    mp, ms = _mask_args(block_mask, B, H, N)
+    st = library().fa_backward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                           _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                           float(scale), int(bool(causal)), mp, ms,
+                                           _ptr(workspace), workspace.numel(),
+                                           ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_blocksparse")
+    return dq, dk, dv
 
 
 def fa_backward_workspace_size(B: int, H: int, N: int, d: int) -> int:

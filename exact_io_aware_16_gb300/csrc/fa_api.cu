@@ -106,8 +106,9 @@ long long fa_forward_tile_count(int N, int causal) {
   return nq * (nq + 1) / 2;  // tiles are square: query tile i visits key tiles 0..i
 }
 
-int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-               int N, int d, float scale, int causal, void* stream) {
+static int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int d, float scale, int causal, const uint8_t* bmask,
+                        long long mstride, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
@@ -132,8 +133,31 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   a.d = d;
   a.scale_log2 = log2e_times(scale);
   a.causal = causal ? 1 : 0;
+  a.bmask = bmask;
+  a.mstride = mstride;
   cudaError_t e = fa::launch_forward(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// block-sparse calls: mask present, at most kMaxSparseTiles tiles, stride >= 0
+static int check_sparse(const uint8_t* bmask, long long mstride, int N) {
+  if (!bmask) return FA_ERR_NULL;
+  if (N > 128 * fa::kMaxSparseTiles || mstride < 0) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, void* stream) {
+  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, 0, stream);
+}
+
+int fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const uint8_t* block_mask, long long mask_head_stride, void* stream) {
+  const int st = check_sparse(block_mask, mask_head_stride, N);
+  if (st != FA_OK) return st;
+  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, mask_head_stride,
+                      stream);
 }
 
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
@@ -156,7 +180,8 @@ int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H
 
 static int bwd_step(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                     float* D, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                    float scale, int causal, void* stream, bool do_dkdv, bool do_dq) {
+                    float scale, int causal, void* stream, bool do_dkdv, bool do_dq,
+                    const uint8_t* bmask = nullptr, long long mstride = 0) {
   if (!q || !k || !v || !dO || !lse || !D) return FA_ERR_NULL;
   if ((do_dkdv && (!dk || !dv)) || (do_dq && !dq)) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
@@ -189,6 +214,8 @@ static int bwd_step(const void* q, const void* k, const void* v, const void* dO,
   a.scale = scale;
   a.scale_log2 = log2e_times(scale);
   a.causal = causal ? 1 : 0;
+  a.bmask = bmask;
+  a.mstride = mstride;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // dQ first: it refines D in place (exact D = sum_j P_ij dP_ij), which the
   // dK / dV kernel then reads.
@@ -211,9 +238,11 @@ int fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, 
                   false, true);
 }
 
-int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+static int backward_impl(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, const uint8_t* bmask,
+                         long long mstride, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
@@ -227,7 +256,26 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   if ((st = check_arch()) != FA_OK) return st;
   float* D = static_cast<float*>(workspace);
   if ((st = fa_backward_preprocess(o, dO, D, B, H, N, d, stream)) != FA_OK) return st;
-  return bwd_step(q, k, v, dO, lse, D, dq, dk, dv, B, H, N, d, scale, causal, stream, true, true);
+  return bwd_step(q, k, v, dO, lse, D, dq, dk, dv, B, H, N, d, scale, causal, stream, true, true,
+                  bmask, mstride);
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr, 0,
+                       workspace, workspace_bytes, stream);
+}
+
+int fa_backward_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, long long mask_head_stride,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_sparse(block_mask, mask_head_stride, N);
+  if (st != FA_OK) return st;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, block_mask,
+                       mask_head_stride, workspace, workspace_bytes, stream);
 }
 
 int fa_get_device_error(void* stream, uint32_t* detail) {

@@ -94,7 +94,10 @@ struct BwdLayout {
   static constexpr uint32_t kStr1 = kStr0 + kStages * kTileBytes;      // [stage] tiles
   static constexpr uint32_t kVec = kStr1 + kStages * kTileBytes;       // lse/D vectors
   static constexpr uint32_t kBar = kVec + 2 * 2 * 128 * 4;
-  static constexpr uint32_t kSmem = kBar + 256 + 1024;
+  static constexpr uint32_t kList = kBar + 256;  // block-sparse tile list (uint16)
+  static constexpr uint32_t kSmemUsed = kList + 2 * kMaxSparseTiles + 1024;
+  // at least 116 KB, so two CTAs never share an SM (each takes all 512 TMEM columns)
+  static constexpr uint32_t kSmem = kSmemUsed > 118784u ? kSmemUsed : 118784u;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = 0;     // S (or S^T); P bf16 packed inside each half
   static constexpr uint32_t kDPCol = 128;  // dP (or dP^T); dS bf16 packed inside each half
@@ -111,7 +114,25 @@ struct BwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int nlist;  // block-sparse: entries of the tile list
 };
+
+// Block-sparse tile list, built by warp 0 with ballots: the tiles t in
+// [t_begin, t_end) for which mask[t * t_stride] != 0 (so t is a query tile
+// for the dK/dV kernel and a key tile for the dQ kernel), in order.
+__device__ __forceinline__ void build_list(uint16_t* list, int* count_out, const uint8_t* mask,
+                                           long long t_stride, int t_begin, int t_end) {
+  const int lane = static_cast<int>(lane_id());
+  int count = 0;
+  for (int base = t_begin; base < t_end; base += 32) {
+    const int t = base + lane;
+    const bool use = t < t_end && mask[t * t_stride] != 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, use);
+    if (use) list[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(t);
+    count += __popc(bal);
+  }
+  if (lane == 0) *count_out = count;
+}
 
 __device__ __forceinline__ bool bwd_warp_wait(uint64_t* bar, uint32_t parity, BwdBars* b,
                                               uint32_t code) {
@@ -177,9 +198,10 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, BwdBars* bars,
                                              int res_row0, const CUtensorMap* s0,
                                              const CUtensorMap* s1, int first_tile, int ntiles,
                                              int bh, const float* lse_bh, const float* D_bh,
-                                             int N) {
+                                             int N, const uint16_t* list) {
   using L = BwdLayout<D>;
   const int lane = static_cast<int>(lane_id());
+  if (ntiles == 0) return;  // nothing to compute: load nothing
   if (lane == 0) {
     tma_prefetch_desc(r0);
     tma_prefetch_desc(r1);
@@ -197,7 +219,7 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, BwdBars* bars,
     const uint32_t ph = (n / kStages) & 1;
     bool ok = mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101);
     if (!__all_sync(0xffffffffu, ok)) break;
-    const int row0 = (first_tile + n) * 128;
+    const int row0 = (list ? static_cast<int>(list[n]) : first_tile + n) * 128;
     if (lse_bh != nullptr) {
       float* vec = reinterpret_cast<float*>(smem + L::kVec) + s * 256;  // [lse2 | D]
 #pragma unroll
@@ -279,7 +301,9 @@ __device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bf
 }
 
 // ============================================================ dK / dV
-template <int D, bool CAUSAL>
+// SPARSE: only the query tiles whose block-mask entry for this key tile is
+// set are visited (a compact list built by warp 0).
+template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq,
                        const __grid_constant__ CUtensorMap tk,
@@ -287,7 +311,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
                        const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
-                       float scale_log2) {
+                       float scale_log2, const uint8_t* __restrict__ bmask, long long mstride) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -304,14 +328,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kt = static_cast<int>(blockIdx.x % nt);
   const int k0 = kt * 128;
   const int i_first = CAUSAL ? kt : 0;
-  const int n_iters = nt - i_first;
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  if (SPARSE && warp == 0)  // column kt of the mask: query tiles i >= i_first
+    build_list(list, &bars->nlist, bmask + bh * mstride + kt, nt, i_first, nt);
 
   if (!bwd_init(bars, warp, L::kTmemCols)) return;
   const uint32_t tmem = bars->tmem_base;
+  const int n_iters = SPARSE ? bars->nlist : nt - i_first;
+  auto it_of = [&](int n) -> int { return SPARSE ? static_cast<int>(list[n]) : i_first + n; };
 
   if (warp == kTmaWarp) {
     bwd_producer<D>(smem, bars, &tk, &tv, k0, &tq, &tdo, i_first, n_iters, bh,
-                    lse + static_cast<size_t>(bh) * N, Dvec + static_cast<size_t>(bh) * N, N);
+                    lse + static_cast<size_t>(bh) * N, Dvec + static_cast<size_t>(bh) * N, N,
+                    SPARSE ? list : nullptr);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
@@ -335,7 +364,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->dp_full);
       };
-      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x201) &&
+      bool ok = n_iters > 0 &&
+                mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x201) &&
                 mbar_wait(&bars->str_full[0], 0, &bars->abort_flag, &g_bwd_error, 0x202);
       tc_fence_after_sync();
       if (ok) {
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t col0 = 64u * g;
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
-      const int it = i_first + n;
+      const int it = it_of(n);
       const int q0 = it * 128;
       // lse * log2(e) and D of this query tile, staged with the tiles
       const float* lse2_s = vec + (n % kStages) * 256;
@@ -460,7 +490,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(&bars->ds_ready);
     }
-    if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x302)) {
+    if (SPARSE && n_iters == 0) {
+      // no query tile keeps this key tile: dK = dV = 0 (tensor memory is never read)
+      if (krow < N) {
+        const size_t off = (static_cast<size_t>(bh) * N + krow) * D;
+        uint4* pk = reinterpret_cast<uint4*>(dk + off + (D == 128 ? col0 : 0));
+        uint4* pv = reinterpret_cast<uint4*>(dv + off + (D == 128 ? col0 : 0));
+        const int nvec = (D == 128 ? 64 : (g == 0 ? 64 : 0)) / 8;
+        for (int e = 0; e < nvec; ++e) {
+          pk[e] = make_uint4(0u, 0u, 0u, 0u);
+          pv[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    } else if (ok && bwd_warp_wait(&bars->acc_done, 0, bars, 0x302)) {
       tc_fence_after_sync();
       const bool valid = krow < N;
       const size_t off = (static_cast<size_t>(bh) * N + (valid ? krow : 0)) * D;
@@ -487,13 +529,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // MMA).  The epilogue corrects dQ = dQ~ - scale (D_i - D~_i) B_i, which removes
 // the error that bf16 rounding of O puts into D~, and writes D_i back over
 // D~_i for the dK/dV kernel that runs next.
-template <int D, bool CAUSAL>
+// SPARSE: only the key tiles this query tile keeps in the block mask are
+// visited (a compact list built by warp 0).
+template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv,
                      const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
                      float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
-                     float scale, float scale_log2) {
+                     float scale, float scale_log2, const uint8_t* __restrict__ bmask,
+                     long long mstride) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -507,15 +552,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = static_cast<int>(blockIdx.x / nt);
   const int qt = nt - 1 - static_cast<int>(blockIdx.x % nt);
   const int q0 = qt * 128;
-  const int n_iters = CAUSAL ? (qt + 1) : nt;
+  const int n_dense = CAUSAL ? (qt + 1) : nt;
   constexpr uint32_t kDQ = L::kAcc0;  // dQ~ accumulator
   constexpr uint32_t kB = L::kAcc1;   // B = P K accumulator
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  if (SPARSE && warp == 0)  // row qt of the mask: key tiles j < n_dense
+    build_list(list, &bars->nlist, bmask + bh * mstride + static_cast<long long>(qt) * nt, 1, 0,
+               n_dense);
 
   if (!bwd_init(bars, warp, L::kTmemCols)) return;
   const uint32_t tmem = bars->tmem_base;
+  const int n_iters = SPARSE ? bars->nlist : n_dense;
+  auto kt_of = [&](int n) -> int { return SPARSE ? static_cast<int>(list[n]) : n; };
 
   if (warp == kTmaWarp) {
-    bwd_producer<D>(smem, bars, &tq, &tdo, q0, &tk, &tv, 0, n_iters, bh, nullptr, nullptr, N);
+    bwd_producer<D>(smem, bars, &tq, &tdo, q0, &tk, &tv, 0, n_iters, bh, nullptr, nullptr, N,
+                    SPARSE ? list : nullptr);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
@@ -539,7 +591,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->dp_full);
       };
-      bool ok = mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x211) &&
+      bool ok = n_iters > 0 &&
+                mbar_wait(&bars->res_full, 0, &bars->abort_flag, &g_bwd_error, 0x211) &&
                 mbar_wait(&bars->str_full[0], 0, &bars->abort_flag, &g_bwd_error, 0x212);
       tc_fence_after_sync();
       if (ok) {
@@ -605,8 +658,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       uint32_t pr[64];
       tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
-      const int kv0 = n * 128;
-      const bool need_mask = (CAUSAL && n == n_iters - 1) || (kv0 + 128 > N);
+      const int kv0 = kt_of(n) * 128;
+      const bool need_mask = (CAUSAL && kv0 + 127 > q0) || (kv0 + 128 > N);
       const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
       const int lim_n = N - 1 - kv0;
       const int lim = need_mask ? (lim_c < lim_n ? lim_c : lim_n) : 0x7fffffff;
@@ -652,6 +705,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars->ds_ready);
+    }
+    if (SPARSE && n_iters == 0) {
+      // no key tile kept: dQ = 0 and the row's D is 0 (tensor memory is never read)
+      if (rvalid) {
+        const size_t off = (static_cast<size_t>(bh) * N + row) * D;
+        uint4* p = reinterpret_cast<uint4*>(dq + off + (D == 128 ? col0 : 0));
+        const int nvec = (D == 128 ? 64 : (g == 0 ? 64 : 0)) / 8;
+        for (int e = 0; e < nvec; ++e) p[e] = make_uint4(0u, 0u, 0u, 0u);
+        if (g == 0) Dvec[static_cast<size_t>(bh) * N + row] = 0.0f;
+      }
+      ok = false;
     }
     // combine the two halves' parts of D (bounded wait)
     if (ok) {
@@ -704,9 +768,9 @@ cudaError_t prep(Kern k, uint32_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPARSE>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, SPARSE>;
   constexpr uint32_t smem = BwdLayout<D>::kSmem;
   cudaError_t e = prep(kern, smem);
   if (e != cudaSuccess) return e;
@@ -714,13 +778,13 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
-      static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2);
+      static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPARSE>
 cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, SPARSE>;
   constexpr uint32_t smem = BwdLayout<D>::kSmem;
   cudaError_t e = prep(kern, smem);
   if (e != cudaSuccess) return e;
@@ -728,8 +792,22 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.BH, a.N,
-      a.scale, a.scale_log2);
+      a.scale, a.scale_log2, a.bmask, a.mstride);
   return cudaGetLastError();
+}
+
+template <bool SPARSE>
+cudaError_t launch_dkdv_s(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 64)
+    return a.causal ? launch_dkdv_t<64, true, SPARSE>(a, s) : launch_dkdv_t<64, false, SPARSE>(a, s);
+  return a.causal ? launch_dkdv_t<128, true, SPARSE>(a, s) : launch_dkdv_t<128, false, SPARSE>(a, s);
+}
+
+template <bool SPARSE>
+cudaError_t launch_dq_s(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 64)
+    return a.causal ? launch_dq_t<64, true, SPARSE>(a, s) : launch_dq_t<64, false, SPARSE>(a, s);
+  return a.causal ? launch_dq_t<128, true, SPARSE>(a, s) : launch_dq_t<128, false, SPARSE>(a, s);
 }
 
 }  // namespace
@@ -749,13 +827,11 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long 
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
-  if (a.d == 64) return a.causal ? launch_dkdv_t<64, true>(a, s) : launch_dkdv_t<64, false>(a, s);
-  return a.causal ? launch_dkdv_t<128, true>(a, s) : launch_dkdv_t<128, false>(a, s);
+  return a.bmask ? launch_dkdv_s<true>(a, s) : launch_dkdv_s<false>(a, s);
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  if (a.d == 64) return a.causal ? launch_dq_t<64, true>(a, s) : launch_dq_t<64, false>(a, s);
-  return a.causal ? launch_dq_t<128, true>(a, s) : launch_dq_t<128, false>(a, s);
+  return a.bmask ? launch_dq_s<true>(a, s) : launch_dq_s<false>(a, s);
 }
 
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s) {

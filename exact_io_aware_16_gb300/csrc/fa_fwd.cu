@@ -62,7 +62,10 @@ struct FwdLayout {
   static constexpr uint32_t kK = kQ + 2 * kTileBytes;
   static constexpr uint32_t kV = kK + kStages * kTileBytes;
   static constexpr uint32_t kBar = kV + kStages * kTileBytes;
-  static constexpr uint32_t kSmem = kBar + 256 + 1024;  // + 1024-byte alignment slack
+  static constexpr uint32_t kList = kBar + 256;  // block-sparse key-tile list (uint16)
+  static constexpr uint32_t kSmemUsed = kList + 2 * kMaxSparseTiles + 1024;  // + align slack
+  // at least 116 KB, so two CTAs never share an SM (each takes all 512 TMEM columns)
+  static constexpr uint32_t kSmem = kSmemUsed > 118784u ? kSmemUsed : 118784u;
   static constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1
   __host__ __device__ static constexpr uint32_t s_col(int g) { return 128u * g; }
   __host__ __device__ static constexpr uint32_t o_col(int g) { return 256u + D * g; }
@@ -76,6 +79,7 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int nlist;  // block-sparse: entries of the key-tile list
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, FwdBars* b,
@@ -89,11 +93,18 @@ __device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity, FwdBars
   return mbar_wait(bar, parity, &b->abort_flag, &g_fwd_error, code);
 }
 
-template <int D, bool CAUSAL>
+// SPARSE: the pair visits only the key tiles that at least one of its two
+// query tiles keeps in the block mask (bmask[bh * mstride + qt * nk + kt] != 0,
+// 128 x 128 tiles).  Warp 0 compacts them into a list in shared memory
+// (entry = key tile | keep-by-tile-0 << 14 | keep-by-tile-1 << 15); for each
+// list entry both query tiles compute their scores, and a query tile that
+// does not keep the key tile masks all of it to -inf.
+template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
-                  float* __restrict__ lse, int BH, int N, float scale_log2) {
+                  float* __restrict__ lse, int BH, int N, float scale_log2,
+                  const uint8_t* __restrict__ bmask, long long mstride) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -136,6 +147,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   __syncthreads();
   if (bars->abort_flag) return;
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  if (SPARSE && warp == 0) {
+    const uint8_t* m0 = bmask + bh * mstride + static_cast<long long>(2 * pair) * nk;
+    const bool has1 = 2 * pair + 1 < nq;  // the pair's second tile may lie past N
+    int count = 0;
+    for (int base = 0; base < nk; base += 32) {
+      const int j = base + lane;
+      bool u0 = false, u1 = false;
+      if (j < nk) {
+        u0 = m0[j] != 0 && (!CAUSAL || j <= 2 * pair);
+        u1 = has1 && m0[nk + j] != 0 && (!CAUSAL || j <= 2 * pair + 1);
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, u0 || u1);
+      if (u0 || u1)
+        list[count + __popc(bal & ((1u << lane) - 1u))] =
+            static_cast<uint16_t>(j | (u0 ? 1 << 14 : 0) | (u1 ? 1 << 15 : 0));
+      count += __popc(bal);
+    }
+    if (lane == 0) bars->nlist = count;
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, L::kTmemCols);
     tmem_relinquish();
@@ -144,10 +175,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+  // number of list positions each query tile runs through (a prefix of the
+  // pair's list), and the key tile at a position
+  const int n0 = SPARSE ? bars->nlist : nkv0;
+  const int n1 = SPARSE ? bars->nlist : nkv1;
+  auto kv_of = [&](int p) -> int { return SPARSE ? (list[p] & 0x3FFF) : p; };
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && n1 > 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
@@ -158,21 +194,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(smem + L::kQ + g * L::kTileBytes + c * 16384, &tq, &bars->q_full, c * 64,
                       (2 * pair + g) * kTileM, bh);
-      for (int j = 0; j < nkv1; ++j) {
+      for (int j = 0; j < n1; ++j) {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
+        const int kt = kv_of(j);
         if (!mbar_wait(&bars->k_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x101)) break;
         mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(smem + L::kK + s * L::kTileBytes + c * 16384, &tk, &bars->k_full[s], c * 64,
-                      j * kTileN, bh);
+                      kt * kTileN, bh);
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x102)) break;
         mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s], c * 64,
-                      j * kTileN, bh);
+                      kt * kTileN, bh);
       }
     }
     __syncwarp();
@@ -201,7 +238,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                   (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->pv_done[g]);
       };
-      bool ok = mma_wait(&bars->q_full, 0, bars, 0x201) &&
+      bool ok = n1 > 0 && mma_wait(&bars->q_full, 0, bars, 0x201) &&
                 mma_wait(&bars->k_full[0], 0, bars, 0x202);
       tc_fence_after_sync();
       if (ok) {
@@ -209,20 +246,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         issue_s(1, 0);
         umma_commit(&bars->k_empty[0]);
       }
-      for (int j = 0; ok && j < nkv1; ++j) {
+      for (int j = 0; ok && j < n1; ++j) {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
         const int sn = (j + 1) % kStages;
         const uint32_t phn = ((j + 1) / kStages) & 1;
         bool v_ready = false, k_next_ready = false;
-        if (j < nkv0) {
+        if (j < n0) {
           ok = mma_wait(&bars->p_ready[0], j & 1, bars, 0x203) &&
                mma_wait(&bars->v_full[s], ph, bars, 0x204);
           if (!ok) break;
           v_ready = true;
           tc_fence_after_sync();
           issue_pv(0, j);
-          if (j + 1 < nkv0) {
+          if (j + 1 < n0) {
             if (!mma_wait(&bars->k_full[sn], phn, bars, 0x205)) { ok = false; break; }
             k_next_ready = true;
             tc_fence_after_sync();
@@ -235,7 +272,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after_sync();
         issue_pv(1, j);
         umma_commit(&bars->v_empty[s]);
-        if (j + 1 < nkv1) {
+        if (j + 1 < n1) {
           if (!k_next_ready && !mma_wait(&bars->k_full[sn], phn, bars, 0x208)) {
             ok = false;
             break;
@@ -253,7 +290,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int g = warp >> 2;           // which query tile of the pair
     const int t = threadIdx.x & 127;   // row within the tile, TMEM lane
     const int row = (2 * pair + g) * kTileM + t;
-    const int nkv = g ? nkv1 : nkv0;
+    const int nkv = g ? n1 : n0;
+    const int q0 = (2 * pair + g) * kTileM;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t scol = tmem + lane_off + L::s_col(g);
     const uint32_t ocol = tmem + lane_off + L::o_col(g);
@@ -273,19 +311,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
       tmem_ld_wait();
       reg_pin(sr);
-      const int kv0 = j * kTileN;
-      const bool need_mask = (CAUSAL && j == nkv - 1) || (kv0 + kTileN > N);
+      const int kv0 = kv_of(j) * kTileN;
+      // a key tile this query tile does not keep: every score is masked
+      const bool keep = !SPARSE || ((list[j] >> (14 + g)) & 1);
+      const bool need_mask = !keep || (CAUSAL && kv0 + kTileN - 1 > q0) || (kv0 + kTileN > N);
       if (need_mask) {
         const int lim_causal = CAUSAL ? (row - kv0) : 0x7fffffff;  // col index <= lim visible
         const int lim_n = N - 1 - kv0;
-        const int lim = lim_causal < lim_n ? lim_causal : lim_n;
+        const int lim = keep ? (lim_causal < lim_n ? lim_causal : lim_n) : -1;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(sr[0]);
+      // row max as a tree of 8 independent partial maxima (short dependency chains)
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      for (int e = 0; e < 8; ++e) mp[e] = __uint_as_float(sr[e]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], __uint_as_float(sr[c + e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_blk = mx * scale_log2;
       // move the running max only when some row of the warp needs it
       const bool move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
@@ -297,15 +344,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      float sum = 0.0f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
       // P~ packed in place: pair c overwrites sr[c], already consumed
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
-        sum += p0 + p1;
+        sp[c & 7] += p0 + p1;
         sr[c] = pack_bf16x2(p0, p1);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       if (move && j > 0) {
@@ -328,9 +376,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive(&bars->p_ready[g]);
     }
     // ------------------------------------------------ epilogue
-    if (ok && warp_wait(&bars->pv_done[g], (nkv - 1) & 1, bars, 0x303)) {
+    if (SPARSE && nkv == 0) {
+      // no key tile at all: O = 0, lse = -inf (tensor memory is never read)
+      if (row < N) {
+        uint4* dst = reinterpret_cast<uint4*>(o + (static_cast<size_t>(bh) * N + row) * D);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+        lse[static_cast<size_t>(bh) * N + row] = -INFINITY;
+      }
+    } else if (ok && warp_wait(&bars->pv_done[g], (nkv - 1) & 1, bars, 0x303)) {
       tc_fence_after_sync();
-      const float inv_l = 1.0f / l_run;
+      // a row with no visible key (block-sparse) has l = 0: O = 0, lse = -inf
+      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
       __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -349,7 +406,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
         }
       }
-      if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_run + log2f(l_run)) * kLn2;
+      if (row < N)
+        lse[static_cast<size_t>(bh) * N + row] =
+            l_run > 0.0f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
   }
 
@@ -372,9 +431,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPARSE>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE>;
   constexpr uint32_t smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -382,15 +441,22 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   const long long blocks = (nq + 1) / 2 * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
-      *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2);
+      *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
+      a.bmask, a.mstride);
   return cudaGetLastError();
+}
+
+template <bool SPARSE>
+cudaError_t launch_forward_s(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 64)
+    return a.causal ? launch_fwd_t<64, true, SPARSE>(a, s) : launch_fwd_t<64, false, SPARSE>(a, s);
+  return a.causal ? launch_fwd_t<128, true, SPARSE>(a, s) : launch_fwd_t<128, false, SPARSE>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
-  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, s) : launch_fwd_t<64, false>(a, s);
-  return a.causal ? launch_fwd_t<128, true>(a, s) : launch_fwd_t<128, false>(a, s);
+  return a.bmask ? launch_forward_s<true>(a, s) : launch_forward_s<false>(a, s);
 }
 
 cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s) {

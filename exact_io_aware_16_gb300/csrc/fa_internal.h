@@ -11,6 +11,7 @@ namespace fa {
 constexpr int kTileM = 128;   // query rows per tile
 constexpr int kTileN = 128;   // key rows per tile
 constexpr int kBoxCols = 64;  // bf16 columns per 128-byte swizzled TMA box
+constexpr int kMaxSparseTiles = 1024;  // block-sparse calls: at most 1024 tiles along N
 
 // A [BH][N][d] bf16 tensor seen by TMA as a 3-D tensor (d, N, BH) with
 // 64-column boxes of 128 rows (resident tiles) or 64 rows (streamed tiles) and
@@ -29,6 +30,8 @@ struct FwdArgs {
   int BH, N, d;
   float scale_log2;  // scale * log2(e)
   int causal;
+  const uint8_t* bmask = nullptr;  // block-sparse mask (nullptr: dense)
+  long long mstride = 0;           // elements between (b,h) masks (0: one shared mask)
 };
 
 struct BwdArgs {
@@ -45,6 +48,8 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   int causal;
+  const uint8_t* bmask = nullptr;  // block-sparse mask (nullptr: dense)
+  long long mstride = 0;
 };
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);

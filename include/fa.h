@@ -152,6 +152,28 @@ int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO
                      int d, float scale, int causal, void* stream);
 
 /*
+ * Block-sparse attention (the talk's block-sparse FlashAttention): exact
+ * attention restricted to the (query tile, key tile) pairs a block mask keeps,
+ * with whole tiles skipped, not computed and masked.
+ *  - block_mask: DEVICE uint8 [nt][nt], nt = ceil(N / 128), row-major; entry
+ *    (i, j) != 0 keeps query rows [128i, 128i+128) x key rows [128j, 128j+128).
+ *  - mask_head_stride: elements between the masks of consecutive (b, h)
+ *    pairs (b*H + h order); 0 = one mask shared by every head.
+ *  - causal applies on top of the mask.  A query row that sees no key has
+ *    o = 0, lse = -inf and dq = 0, and adds nothing to dk, dv.
+ *  - N <= 131072 (at most 1024 tiles); larger N returns FA_ERR_SHAPE.
+ * All other arguments, layouts and errors as for fa_forward / fa_backward.
+ */
+int fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const uint8_t* block_mask, long long mask_head_stride, void* stream);
+int fa_backward_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, long long mask_head_stride,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library timed out in a pipeline wait since the last call (and clears
  * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.

@@ -59,6 +59,12 @@ def check_bf16(name: str, got, ref, report: list | None = None):
 
 def check_lse(name: str, got, ref, report: list | None = None):
     got = to_np(got).reshape(ref.shape)
+    ref = np.asarray(ref, dtype=np.float64)
+    # rows with no visible key (block-sparse) have lse = -inf on both sides
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf_ref), f"{name}: -inf rows differ"
+    got = np.where(inf_ref, 0.0, got)
+    ref = np.where(inf_ref, 0.0, ref)
     err = np.abs(got - ref)
     max_abs = float(err.max()) if err.size else 0.0
     line = f"{name}: max_abs={max_abs:.3e}"

@@ -86,6 +86,18 @@ def test_backward_validation(lib):
     assert bwd(lib, dk=FAKE + 4) == -4
 
 
+def test_blocksparse_validation(lib):
+    f = lib.fa_forward_blocksparse
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 0.125, 0, None, 0, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 0.125, 0, FAKE, -5, None) == -2
+    # more than 1024 tiles along N
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128 * 1024 + 1, 64, 0.125, 0, FAKE, 0,
+             None) == -2
+    g = lib.fa_backward_blocksparse
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 0.125, 0,
+             None, 0, FAKE * 16, 1 << 20, None) == -1
+
+
 def test_workspace_size_is_linear_in_n(lib):
     f = lib.fa_backward_workspace_size
     assert f(1, 1, 0, 64) == 0
