@@ -210,6 +210,36 @@ def run_reference(args, world, rank):
     return 0
 
 
+def band_mask(spec: str, N: int):
+    """Block mask [nt, nt] from 'band:W[:G]': keep tiles with |i - j| <= W and
+    the first G tile rows and columns (local band + global tokens)."""
+    parts = spec.split(":")
+    if parts[0] != "band" or len(parts) not in (2, 3):
+        raise ValueError("block mask spec must be band:W[:G]")
+    W = int(parts[1])
+    G = int(parts[2]) if len(parts) == 3 else 0
+    nt = -(-N // 128)
+    i = torch.arange(nt)[:, None]
+    j = torch.arange(nt)[None, :]
+    return (((i - j).abs() <= W) | (i < G) | (j < G)).to(torch.uint8)
+
+
+def kept_elements(mask, N: int, causal: bool) -> float:
+    """Score elements (query, key) that a block mask and the causal mask keep."""
+    nt = mask.shape[0]
+    rows = [min(128, N - 128 * t) for t in range(nt)]
+    total = 0.0
+    for i in range(nt):
+        for j in range(nt):
+            if not mask[i, j] or (causal and j > i):
+                continue
+            if causal and j == i:
+                total += rows[i] * (rows[i] + 1) / 2
+            else:
+                total += rows[i] * rows[j]
+    return total
+
+
 def workload_config(w, causal):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
             "scale": w.scale, "qk_mult": w.qk_mult, "seed": w.seed,
@@ -236,6 +266,8 @@ def run_ours(args, world, rank, local):
     D = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
+    if args.block_mask:
+        return run_sparse(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
     names = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
 
     def step(ev=None):
@@ -393,6 +425,71 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
+    """Block-sparse step: fa_forward_blocksparse + fa_backward_blocksparse."""
+    q, k, v, dO = tensors
+    mask_cpu = band_mask(args.block_mask, w.N)
+    mask = mask_cpu.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_backward_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+
+    def step(ev=None):
+        fa.fa_forward_blocksparse(q, k, v, mask, causal=causal, scale=w.scale, o=o, lse=lse,
+                                  stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_backward_blocksparse(q, k, v, o, dO, lse, mask, causal=causal, scale=w.scale,
+                                   dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    for s_ in range(args.steps):
+        evs[s_][0].record(stream)
+        step(evs[s_])
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    ms = max_over_ranks(fwd_ms + bwd_ms, world)
+    E = kept_elements(mask_cpu, w.N, causal) * w.B * w.H
+    f_fwd, f_bwd = 4.0 * w.d * E, 10.0 * w.d * E
+    peaks, peak_src = read_peaks()
+    peak = peaks["bf16_tflops"]
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    if rank == 0:
+        dense = w.B * w.H * w.N * w.N * (0.5 if causal else 1.0)
+        cfg = workload_config(w, causal)
+        cfg.update({"block_mask": args.block_mask, "kept_fraction": E / dense})
+        line = {
+            "metric": METRIC + " (block-sparse, FLOPs of kept tiles)",
+            "value": world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg, "fwd_tflops": fwd_tf,
+            "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "kernel": "fwd", "achieved": fwd_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": fwd_tf / peak, "traffic": None,
+                         "peak_kind": f"burst bf16 ({peak_src})"},
+            "gpu_launches": 4 * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,6 +498,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--causal", type=int, default=None, help="override the workload's mask mode")
+    ap.add_argument("--block-mask", default=None,
+                    help="time the block-sparse path with mask band:W[:G] (tiles of 128)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
