@@ -20,6 +20,9 @@ What each function follows:
   06:52-07:24 and 08:26).
 * ``online_softmax`` / ``online_attention_row``: the running-max update of
   transcript 04:46-05:17, used only to pin online == two-pass.
+* ``decode``: the same definition for Nq query rows against an Nk-row key /
+  value cache (the transcript's closing mention of KV caches, 11:33), query i
+  at cache position Nk - Nq + i for the causal mask.
 * ``mask=`` (block-sparse, the talk's block-sparse FlashAttention): scores of
   dropped (query block, key block) pairs are -inf; a row with no visible key
   is defined as o = 0, lse = -inf with zero gradients.
@@ -119,6 +122,8 @@ class Oracle:
                                                 ip, i64, dp, dp, i]
         lib.fa_oracle_online_softmax.argtypes = [dp, i, i, dp, dp]
         lib.fa_oracle_online_attention_row.argtypes = [dp, dp, i, i, i, dp, dp]
+        lib.fa_oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, d, i, dp, dp, i]
+        lib.fa_oracle_decode.restype = ctypes.c_int
         lib.fa_oracle_set_block_mask.argtypes = [ctypes.c_void_p, i, i, i, i64]
         lib.fa_oracle_set_block_mask.restype = None
         for f in (lib.fa_oracle_forward, lib.fa_oracle_backward_rows,
@@ -234,6 +239,27 @@ class Oracle:
                                     mask=mask, block=block)
         return dq, dk, dv, (m, l, D, D_alt)
 
+    def decode(self, q, k, v, scale: float, causal: bool, nthreads: int | None = None):
+        """A few queries against a key/value cache: q [..., Nq, d], k, v [..., Nk, d].
+
+        Query i sits at cache position Nk - Nq + i; with causal it sees keys up
+        to that position.  Returns (o [BH*Nq, d], lse [BH*Nq]).
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        d = q.shape[-1]
+        Nq, Nk = q.shape[-2], k.shape[-2]
+        BH = int(np.prod(q.shape[:-2]))
+        if k.shape != v.shape or int(np.prod(k.shape[:-2])) != BH or k.shape[-1] != d:
+            raise ValueError("q, k, v shapes disagree")
+        o = np.empty((BH * Nq, d), np.float64)
+        lse = np.empty((BH * Nq,), np.float64)
+        rc = self.lib.fa_oracle_decode(_ptr(q), _ptr(k), _ptr(v), BH, Nq, Nk, d, float(scale),
+                                       int(bool(causal)), _ptr(o), _ptr(lse),
+                                       int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"fa_oracle_decode failed ({rc})")
+        return o, lse
+
     def online_softmax(self, x, block: int):
         """Running (m, l) after each block of the row x (online update)."""
         x = _f64(x).reshape(-1)
@@ -288,6 +314,10 @@ def backward(*a, **kw):
 
 def online_softmax(*a, **kw):
     return default().online_softmax(*a, **kw)
+
+
+def decode(*a, **kw):
+    return default().decode(*a, **kw)
 
 
 def online_attention_row(*a, **kw):

@@ -339,6 +339,66 @@ int fa_oracle_backward_cols(const double* q, const double* k, const double* v, c
 }
 
 /* ------------------------------------------------------------------ */
+/* decode: a few queries against a long key/value cache                 */
+
+typedef struct {
+  const double *q, *k, *v;
+  int Nq, Nk, d, causal;
+  double scale;
+  double *o, *lse;
+} dec_t;
+
+/* Query i of a decode step sits at cache position Nk - Nq + i (the new tokens
+ * are the last Nq positions); with the causal mask it sees keys 0 .. that
+ * position.  The row is the plain definition: scores, safe softmax, P V. */
+static void dec_item(void* ctx, int64_t it, double* s) {
+  const dec_t* J = (const dec_t*)ctx;
+  const int64_t bh = it / J->Nq;
+  const int i = (int)(it % J->Nq);
+  const int Nk = J->Nk, d = J->d;
+  const int last = J->causal ? Nk - J->Nq + i : Nk - 1;
+  const double* qi = J->q + ((size_t)bh * J->Nq + i) * d;
+  double m = -INFINITY;
+  for (int j = 0; j < Nk; ++j) {
+    if (j > last) {
+      s[j] = -INFINITY;
+      continue;
+    }
+    const double* kj = J->k + ((size_t)bh * Nk + j) * d;
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qi[c] * kj[c];
+    s[j] = J->scale * acc;
+    if (s[j] > m) m = s[j];
+  }
+  double* oi = J->o + (size_t)it * d;
+  for (int c = 0; c < d; ++c) oi[c] = 0.0;
+  if (m == -INFINITY) { /* no visible key */
+    J->lse[it] = -INFINITY;
+    return;
+  }
+  double l = 0.0;
+  for (int j = 0; j < Nk; ++j) l += exp(s[j] - m);
+  for (int j = 0; j < Nk; ++j) {
+    const double p = exp(s[j] - m) / l;
+    if (p == 0.0) continue;
+    const double* vj = J->v + ((size_t)bh * Nk + j) * d;
+    for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
+  }
+  J->lse[it] = m + log(l);
+}
+
+/* q [BH][Nq][d], k and v [BH][Nk][d]; o [BH][Nq][d], lse [BH][Nq]. */
+int fa_oracle_decode(const double* q, const double* k, const double* v, int BH, int Nq, int Nk,
+                     int d, double scale, int causal, double* o, double* lse, int nthreads) {
+  if (!q || !k || !v || !o || !lse || BH < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+  dec_t J;
+  J.q = q; J.k = k; J.v = v;
+  J.Nq = Nq; J.Nk = Nk; J.d = d; J.causal = causal; J.scale = scale;
+  J.o = o; J.lse = lse;
+  return run_pool(dec_item, &J, (int64_t)BH * Nq, (size_t)Nk, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
 /* online-softmax helpers, used only to pin the online update against
  * the two-pass definition ("What is Flash Attention?", 04:46-05:17).    */
 

@@ -406,6 +406,54 @@ def pin_block_mask(orc):
     _close(dv, g[2], 1e-12, atol=1e-14, what="dV without the dropped rows")
 
 
+# ---------------------------------------------------------------- pin 11
+def pin_decode(orc):
+    """Decode (a few queries against a key/value cache):
+    * with Nq = Nk it is the square definition (causal alignments coincide);
+    * against PyTorch's fp64 SDPA with the explicit mask "query i sees keys
+      up to Nk - Nq + i", for Nq < Nk;
+    * splitting the keys into two ranges and merging the two partial results
+      with the running-max update (transcript 04:46-05:17: new max, the two
+      rescale factors, summed and renormalised) gives the whole result;
+    * one key: o = v and lse = scale q.k."""
+    rng = _rng(11)
+    BH, d, scale = 3, 16, 0.25
+    q, k, v = (rng.standard_normal((BH, 40, d)) for _ in range(3))
+    for causal in (False, True):
+        a = orc.forward(q, k, v, scale, causal)
+        b = orc.decode(q, k, v, scale, causal)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    Nq, Nk = 5, 37
+    q = rng.standard_normal((BH, Nq, d))
+    k, v = (rng.standard_normal((BH, Nk, d)) for _ in range(2))
+    for causal in (False, True):
+        mask = np.ones((Nq, Nk), dtype=bool)
+        if causal:
+            mask = np.arange(Nk)[None, :] <= (Nk - Nq + np.arange(Nq))[:, None]
+        tq, tk, tv = (torch.tensor(x) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv,
+                                                             attn_mask=torch.tensor(mask),
+                                                             scale=scale)
+        sc = (tq @ tk.transpose(-1, -2)) * scale
+        tlse = torch.logsumexp(sc.masked_fill(~torch.tensor(mask), -math.inf), dim=-1)
+        o, lse = orc.decode(q, k, v, scale, causal)
+        _close(o, to.reshape(-1, d).numpy(), 1e-12, atol=1e-14, what="decode O vs sdpa")
+        _close(lse, tlse.reshape(-1).numpy(), 1e-13, atol=1e-14, what="decode lse vs sdpa")
+    # split the cache at a = 15 and merge
+    a_ = 15
+    o, lse = orc.decode(q, k, v, scale, False)
+    o1, l1 = orc.decode(q, k[:, :a_], v[:, :a_], scale, False)
+    o2, l2 = orc.decode(q, k[:, a_:], v[:, a_:], scale, False)
+    m = np.maximum(l1, l2)
+    w1, w2 = np.exp(l1 - m), np.exp(l2 - m)
+    merged = (w1[:, None] * o1 + w2[:, None] * o2) / (w1 + w2)[:, None]
+    _close(merged, o, 1e-12, atol=1e-14, what="split-merge O")
+    _close(m + np.log(w1 + w2), lse, 1e-13, atol=1e-14, what="split-merge lse")
+    o, lse = orc.decode(q[:, :1], k[:, :1], v[:, :1], scale, True)
+    _close(o, v[:, 0], 1e-15, what="one-key O")
+    _close(lse, scale * np.sum(q[:, 0] * k[:, 0], axis=1), 1e-13, atol=1e-15, what="one-key lse")
+
+
 ALL_PINS = [pin_worked_example, pin_zero_query, pin_one_hot, pin_permutation,
             pin_online_equals_two_pass, pin_finite_differences, pin_structure,
-            pin_torch_sdpa, pin_selection_consistency, pin_block_mask]
+            pin_torch_sdpa, pin_selection_consistency, pin_block_mask, pin_decode]

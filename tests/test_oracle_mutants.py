@@ -36,6 +36,10 @@ MUTANTS = [
     ("block_mask_ignored", "if (J->bmask && !J->bmask[", "if (0 && !J->bmask["),
     ("block_mask_axes_swapped", "(int64_t)(i / J->bq) * J->nkb + j / J->bk]",
      "(int64_t)(j / J->bq) * J->nkb + i / J->bk]"),
+    ("decode_causal_top_left", "const int last = J->causal ? Nk - J->Nq + i : Nk - 1;",
+     "const int last = J->causal ? i : Nk - 1;"),
+    ("decode_dot_uses_v", "const double* kj = J->k + ((size_t)bh * Nk + j) * d;",
+     "const double* kj = J->v + ((size_t)bh * Nk + j) * d;"),
     ("block_mask_ignores_head", "J->bmask[bh * J->mstride +", "J->bmask[0 * J->mstride +"),
 ]
 
