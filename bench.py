@@ -268,6 +268,8 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     if args.block_mask:
         return run_sparse(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
+    if args.decode:
+        return run_decode(args, world, rank, local, fa, w, (q, k, v), stream, dev)
     names = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
 
     def step(ev=None):
@@ -490,6 +492,65 @@ def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     return 0
 
 
+def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
+    """Decode step: the last --decode query rows against the whole key/value
+    cache of the workload (causal: query i at position N - Nq + i).  HBM-bound:
+    reported as GB/s of algorithmic bytes (K, V, q read once; o, lse written)."""
+    q_full, k, v = tensors
+    Nq = int(args.decode)
+    q = q_full[:, :, w.N - Nq:].contiguous()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_size(w.B, w.H, Nq, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    # inputs larger than L2 between steps: rotate over copies of the cache
+    copies = max(1, int((300e6 // (2 * k.numel() * 2)) + 1))
+    caches = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
+
+    def step(i):
+        kk, vv = caches[i % len(caches)]
+        fa.fa_decode(q, kk, vv, causal=True, scale=w.scale, o=o, lse=lse, workspace=ws,
+                     stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    nbytes = (2 * k.numel() + 2 * q.numel()) * 2 + lse.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, peak_src = read_peaks()
+    if rank == 0:
+        cfg = {"workload": f"decode_q{Nq}_{w.name}", "B": w.B, "H": w.H, "Nq": Nq, "Nk": w.N,
+               "d": w.d, "causal": True,
+               "l2": f"{len(caches)} rotating copies of the K/V cache ({2 * k.numel() * 2 / 1e6:.0f} MB each)"}
+        line = {
+            "metric": "attention decode step HBM GB/s (K/V cache read once)", "value": world * gbs,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "kernel": "decode_split+combine", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_kind": peak_src},
+            "gpu_launches": 2 * args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -500,6 +561,8 @@ def main():
     ap.add_argument("--causal", type=int, default=None, help="override the workload's mask mode")
     ap.add_argument("--block-mask", default=None,
                     help="time the block-sparse path with mask band:W[:G] (tiles of 128)")
+    ap.add_argument("--decode", type=int, default=None,
+                    help="time the decode step with this many query rows (<= 16)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

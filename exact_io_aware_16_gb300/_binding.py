@@ -60,6 +60,10 @@ def library():
         lib.fa_backward_blocksparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
                                                 i, vp, ll, vp, sz, vp]
         lib.fa_backward_blocksparse.restype = i
+        lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.fa_decode_workspace_size.restype = sz
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+        lib.fa_decode.restype = i
         lib.fa_backward_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.fa_backward_preprocess.restype = i
         lib.fa_backward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i,
@@ -184,6 +188,34 @@ def fa_backward_blocksparse(q, k, v, o, dO, lse, block_mask, causal: bool = Fals
     if st != FA_OK:
         raise FaError(st, "fa_backward_blocksparse")
     return dq, dk, dv
+
+
+def fa_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(library().fa_decode_workspace_size(B, H, Nq, Nk, d))
+
+
+def fa_decode(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+              workspace=None, stream=None):
+    """Nq (<= 16) query rows q [B,H,Nq,d] against a key/value cache k, v [B,H,Nk,d]."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (B, H, Nk, d))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, d))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, Nq, d))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    need = fa_decode_workspace_size(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = library().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                             float(scale), int(bool(causal)), _ptr(workspace), workspace.numel(),
+                             ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode")
+    return o, lse
 
 
 def fa_backward_workspace_size(B: int, H: int, N: int, d: int) -> int:

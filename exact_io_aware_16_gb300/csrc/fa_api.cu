@@ -278,6 +278,60 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
                        mask_head_stride, workspace, workspace_bytes, stream);
 }
 
+static int check_decode_shape(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || Nq > fa::kMaxDecodeQueries) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  const long long total = static_cast<long long>(B) * H * Nk * d;
+  if (total >= (1ll << 31)) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode_shape(B, H, Nq, Nk, d) != FA_OK) return 0;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long S = fa::decode_splits(BH, Nk);
+  const size_t floats = static_cast<size_t>(BH * S * Nq) * (d + 1);
+  return (floats * sizeof(float) + 512 + 255) & ~static_cast<size_t>(255);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  int st = check_decode_shape(B, H, Nq, Nk, d);
+  if (st != FA_OK) return st;
+  if (causal && Nk < Nq) return FA_ERR_SHAPE;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!workspace || workspace_bytes < fa_decode_workspace_size(B, H, Nq, Nk, d) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  fa::DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.BH = B * H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.S = fa::decode_splits(a.BH, Nk);
+  a.chunk = ((Nk + a.S - 1) / a.S + 63) / 64 * 64;
+  a.S = (Nk + a.chunk - 1) / a.chunk;  // no empty ranges
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  const size_t n_o = static_cast<size_t>(a.BH) * a.S * Nq * d;
+  a.part_o = static_cast<float*>(workspace);
+  // partial lse after the partial outputs, 256-byte aligned
+  a.part_lse = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(a.part_o + n_o) + 255) & ~static_cast<uintptr_t>(255));
+  cudaError_t e = fa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_get_device_error(void* stream, uint32_t* detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t w_fwd = 0, w_bwd = 0;

@@ -12,6 +12,7 @@ constexpr int kTileM = 128;   // query rows per tile
 constexpr int kTileN = 128;   // key rows per tile
 constexpr int kBoxCols = 64;  // bf16 columns per 128-byte swizzled TMA box
 constexpr int kMaxSparseTiles = 1024;  // block-sparse calls: at most 1024 tiles along N
+constexpr int kMaxDecodeQueries = 16;  // decode calls: at most 16 query rows
 
 // A [BH][N][d] bf16 tensor seen by TMA as a 3-D tensor (d, N, BH) with
 // 64-column boxes of 128 rows (resident tiles) or 64 rows (streamed tiles) and
@@ -52,7 +53,32 @@ struct BwdArgs {
   long long mstride = 0;
 };
 
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  float* part_o;    // workspace: [BH][S][Nq][d] partial outputs
+  float* part_lse;  // workspace: [BH][S][Nq] partial lse
+  int BH, Nq, Nk, d, S, chunk;
+  float scale;
+  int causal;
+};
+
+// Number of key ranges a decode step is split into (shape-only, so the
+// workspace size needs no device): enough CTAs for four waves of 152 SMs,
+// ranges of at least 256 keys.
+inline int decode_splits(long long BH, int Nk) {
+  const long long by_len = (Nk + 255) / 256;
+  long long by_sms = (608 + BH - 1) / BH;
+  if (by_sms < 1) by_sms = 1;
+  const long long s = by_len < by_sms ? by_len : by_sms;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                   cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);

@@ -174,6 +174,23 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Decode step: Nq new query rows against an Nk-row key/value cache (the KV
+ * cache the transcript of "What is Flash Attention?" names as the next stop,
+ * 11:33).  q [B][H][Nq][d], k and v [B][H][Nk][d] bf16; o [B][H][Nq][d] bf16,
+ * lse [B][H][Nq] fp32.  Query i sits at cache position Nk - Nq + i: with
+ * causal != 0 it sees keys 0 .. Nk - Nq + i, else all Nk keys.  1 <= Nq <= 16,
+ * Nk >= 1 (Nk >= Nq when causal), d in {64, 128}.  The key axis is split into
+ * ranges processed in parallel, merged by the online-softmax update; the
+ * workspace (device memory, 256-byte aligned, contents irrelevant) holds the
+ * partial results: fa_decode_workspace_size() bytes.  Errors as fa_forward,
+ * FA_ERR_WORKSPACE for a missing or small workspace.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library timed out in a pipeline wait since the last call (and clears
  * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.

@@ -98,6 +98,24 @@ def test_blocksparse_validation(lib):
              None, 0, FAKE * 16, 1 << 20, None) == -1
 
 
+def test_decode_validation(lib):
+    ws = lib.fa_decode_workspace_size(2, 4, 8, 1000, 128)
+    assert ws > 0 and ws % 256 == 0
+    assert lib.fa_decode_workspace_size(1, 1, 17, 1000, 128) == 0  # Nq > 16
+    assert lib.fa_decode_workspace_size(1, 1, 4, 1000, 96) == 0
+
+    def dec(Nq=4, Nk=100, d=64, causal=0, w=FAKE * 16, wb=1 << 24, q=FAKE):
+        return lib.fa_decode(q, FAKE, FAKE, FAKE, FAKE, 1, 2, Nq, Nk, d, 0.125, causal, w, wb,
+                             None)
+
+    assert dec(q=None) == -1
+    assert dec(Nq=17) == -2
+    assert dec(Nq=8, Nk=4, causal=1) == -2  # causal needs Nk >= Nq
+    assert dec(d=32) == -3
+    assert dec(w=None) == -6
+    assert dec(wb=16) == -6
+
+
 def test_workspace_size_is_linear_in_n(lib):
     f = lib.fa_backward_workspace_size
     assert f(1, 1, 0, 64) == 0
