@@ -26,6 +26,11 @@ What each function follows:
 * ``mask=`` (block-sparse, the talk's block-sparse FlashAttention): scores of
   dropped (query block, key block) pairs are -inf; a row with no visible key
   is defined as o = 0, lse = -inf with zero gradients.
+* ``dropout=(p, seed, offset)`` (the talk's dropout on P before the product
+  with V, transcript Q&A after 10:00): O = (P o Z / (1 - p)) V, lse that of
+  P.  Z is drawn by Philox4x32-10 (Salmon et al., SC 2011) at counter
+  (j // 4, i, bh, offset) with key seed, word j % 4; an element is kept iff
+  that word is >= floor(p * 2^32).
 
 Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
 """
@@ -126,6 +131,13 @@ class Oracle:
         lib.fa_oracle_decode.restype = ctypes.c_int
         lib.fa_oracle_set_block_mask.argtypes = [ctypes.c_void_p, i, i, i, i64]
         lib.fa_oracle_set_block_mask.restype = None
+        lib.fa_oracle_set_dropout.argtypes = [i, ctypes.c_uint64, ctypes.c_uint32,
+                                              ctypes.c_uint32, d]
+        lib.fa_oracle_set_dropout.restype = None
+        lib.fa_oracle_dropout_word.argtypes = [ctypes.c_uint64, ctypes.c_uint32, i64, i, i]
+        lib.fa_oracle_dropout_word.restype = ctypes.c_uint32
+        lib.fa_oracle_philox4x32_10.argtypes = [ctypes.c_void_p] * 3
+        lib.fa_oracle_philox4x32_10.restype = None
         for f in (lib.fa_oracle_forward, lib.fa_oracle_backward_rows,
                   lib.fa_oracle_backward_cols, lib.fa_oracle_online_softmax,
                   lib.fa_oracle_online_attention_row):
@@ -133,16 +145,23 @@ class Oracle:
         self.lib = lib
         self.path = lib_path
 
-    def _masked(self, mask, block, BH):
-        """Context manager that installs a block mask for the calls inside it.
+    def _masked(self, mask, block, BH, dropout=None):
+        """Context manager that installs a block mask and / or dropout for the
+        calls inside it.
 
         mask: uint8 array [nqb, nkb] (shared by every (b,h)) or [BH, nqb, nkb];
         nonzero keeps the (query block, key block) pair.  block = (bq, bk) rows.
+        dropout: None or (p, seed, offset); see ``dropout_params``.
         """
         lib = self.lib
 
         class _Ctx:
             def __enter__(ctx):
+                if dropout is not None:
+                    pd, seed, offset = dropout
+                    thr, rs = dropout_params(pd)
+                    lib.fa_oracle_set_dropout(1, int(seed) & (2**64 - 1),
+                                              int(offset) & 0xFFFFFFFF, thr, rs)
                 if mask is None:
                     return ctx
                 m = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
@@ -158,12 +177,13 @@ class Oracle:
 
             def __exit__(ctx, *exc):
                 lib.fa_oracle_set_block_mask(None, 1, 1, 0, 0)
+                lib.fa_oracle_set_dropout(0, 0, 0, 0, 1.0)
                 return False
 
         return _Ctx()
 
     def forward(self, q, k, v, scale: float, causal: bool, rows=None,
-                nthreads: int | None = None, mask=None, block=(128, 128)):
+                nthreads: int | None = None, mask=None, block=(128, 128), dropout=None):
         """O and lse of the definition.
 
         q, k, v: [B,H,N,d] or [BH,N,d] (any dtype; converted exactly to float64).
@@ -175,7 +195,7 @@ class Oracle:
         sel, n = _sel(rows, BH, N)
         o = np.empty((n, d), np.float64)
         lse = np.empty((n,), np.float64)
-        with self._masked(mask, block, BH):
+        with self._masked(mask, block, BH, dropout):
             rc = self.lib.fa_oracle_forward(
                 _ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale), int(bool(causal)),
                 _iptr(sel), n, _ptr(o), _ptr(lse), int(nthreads or default_threads()))
@@ -184,7 +204,8 @@ class Oracle:
         return o, lse
 
     def backward_rows(self, q, k, v, dO, scale: float, causal: bool, rows=None,
-                      nthreads: int | None = None, mask=None, block=(128, 128)):
+                      nthreads: int | None = None, mask=None, block=(128, 128),
+                      dropout=None):
         """Row pass: dq for the selected rows plus per-row m, l, D and D_alt.
 
         D is sum_j P_ij dP_ij; D_alt is sum_c dO_ic O_ic.  They agree exactly in
@@ -198,7 +219,7 @@ class Oracle:
         l = np.empty((n,), np.float64)
         D = np.empty((n,), np.float64)
         D_alt = np.empty((n,), np.float64)
-        with self._masked(mask, block, BH):
+        with self._masked(mask, block, BH, dropout):
             rc = self.lib.fa_oracle_backward_rows(
                 _ptr(q), _ptr(k), _ptr(v), _ptr(dO), BH, N, d, float(scale), int(bool(causal)),
                 _iptr(sel), n, _ptr(dq), _ptr(m), _ptr(l), _ptr(D), _ptr(D_alt),
@@ -208,7 +229,8 @@ class Oracle:
         return dq, m, l, D, D_alt
 
     def backward_cols(self, q, k, v, dO, m_all, l_all, D_all, scale: float, causal: bool,
-                      cols=None, nthreads: int | None = None, mask=None, block=(128, 128)):
+                      cols=None, nthreads: int | None = None, mask=None, block=(128, 128),
+                      dropout=None):
         """Column pass: dk, dv for the selected key rows (flat bh*N + j).
 
         m_all, l_all, D_all must cover every row (from backward_rows(rows=None)).
@@ -221,7 +243,7 @@ class Oracle:
         sel, n = _sel(cols, BH, N)
         dk = np.empty((n, d), np.float64)
         dv = np.empty((n, d), np.float64)
-        with self._masked(mask, block, BH):
+        with self._masked(mask, block, BH, dropout):
             rc = self.lib.fa_oracle_backward_cols(
                 _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(m_all), _ptr(l_all), _ptr(D_all),
                 BH, N, d, float(scale), int(bool(causal)), _iptr(sel), n, _ptr(dk), _ptr(dv),
@@ -231,12 +253,12 @@ class Oracle:
         return dk, dv
 
     def backward(self, q, k, v, dO, scale: float, causal: bool, nthreads: int | None = None,
-                 mask=None, block=(128, 128)):
+                 mask=None, block=(128, 128), dropout=None):
         """Full backward: (dq, dk, dv) each [BH*N, d], plus (m, l, D, D_alt) per row."""
         dq, m, l, D, D_alt = self.backward_rows(q, k, v, dO, scale, causal, None, nthreads,
-                                                mask=mask, block=block)
+                                                mask=mask, block=block, dropout=dropout)
         dk, dv = self.backward_cols(q, k, v, dO, m, l, D, scale, causal, None, nthreads,
-                                    mask=mask, block=block)
+                                    mask=mask, block=block, dropout=dropout)
         return dq, dk, dv, (m, l, D, D_alt)
 
     def decode(self, q, k, v, scale: float, causal: bool, nthreads: int | None = None):
@@ -259,6 +281,31 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"fa_oracle_decode failed ({rc})")
         return o, lse
+
+    def philox(self, ctr, key):
+        """Philox4x32-10 of a 4-word counter and a 2-word key (4 words out)."""
+        c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+        kk = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+        if c.shape != (4,) or kk.shape != (2,):
+            raise ValueError("counter has 4 words, key 2")
+        out = np.zeros(4, np.uint32)
+        self.lib.fa_oracle_philox4x32_10(c.ctypes.data, kk.ctypes.data, out.ctypes.data)
+        return [int(x) for x in out]
+
+    def dropout_word(self, seed: int, offset: int, bh: int, i: int, j: int) -> int:
+        """The 32-bit uniform word that decides element (i, j) of head bh."""
+        return int(self.lib.fa_oracle_dropout_word(int(seed) & (2**64 - 1),
+                                                   int(offset) & 0xFFFFFFFF, int(bh),
+                                                   int(i), int(j)))
+
+    def dropout_keep(self, p: float, seed: int, offset: int, bh: int, n_rows: int, n_cols: int):
+        """Keep matrix Z [n_rows, n_cols] (bool) of head bh."""
+        thr, _ = dropout_params(p)
+        z = np.empty((n_rows, n_cols), dtype=bool)
+        for i in range(n_rows):
+            for j in range(n_cols):
+                z[i, j] = self.dropout_word(seed, offset, bh, i, j) >= thr
+        return z
 
     def online_softmax(self, x, block: int):
         """Running (m, l) after each block of the row x (online update)."""
@@ -285,6 +332,19 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"fa_oracle_online_attention_row failed ({rc})")
         return o, float(lse[0])
+
+
+def dropout_params(p: float):
+    """(thr, rs) of a dropout probability p in [0, 1).
+
+    p is first rounded to IEEE single (the precision the library takes it
+    in); an element is kept iff its 32-bit word is >= thr = floor(p * 2^32),
+    and kept values are scaled by rs = 1 / (1 - p).
+    """
+    p32 = float(np.float32(p))
+    if not 0.0 <= p32 < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return int(np.floor(p32 * 4294967296.0)), 1.0 / (1.0 - p32)
 
 
 def default() -> Oracle:
@@ -322,3 +382,11 @@ def decode(*a, **kw):
 
 def online_attention_row(*a, **kw):
     return default().online_attention_row(*a, **kw)
+
+
+def dropout_word(*a, **kw):
+    return default().dropout_word(*a, **kw)
+
+
+def dropout_keep(*a, **kw):
+    return default().dropout_keep(*a, **kw)

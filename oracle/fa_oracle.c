@@ -37,6 +37,10 @@
  *    skipped; their scores are -inf, which is exact attention restricted to
  *    the kept blocks.  A row with no visible key has no softmax; it is defined
  *    here as o = 0, lse = -inf and zero gradients.
+ *  - dropout (the talk: dropout applied to P before the product with V):
+ *    O = (P o Z / (1 - p)) V with Z_ij in {0, 1} drawn by the counter-based
+ *    Philox4x32-10 generator (see philox4x32_10), so the same Z can be
+ *    replayed exactly; lse is that of P (before dropout).
  *
  * Layout: every [BH][N][d] array is row-major with index (bh*N + i)*d + c.
  * Row / column selections are flat indices r = bh*N + i.
@@ -47,6 +51,42 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* Philox4x32-10 counter-based generator (Salmon, Moraes, Dror, Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten rounds of
+ * two 32x32->64 multiplications mixed with the other counter words and the
+ * key; the key is bumped by the two Weyl constants between rounds. */
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * x0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * x2;
+    const uint32_t y0 = (uint32_t)(p1 >> 32) ^ x1 ^ k0;
+    const uint32_t y1 = (uint32_t)p1;
+    const uint32_t y2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
+    const uint32_t y3 = (uint32_t)p0;
+    x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* The generator itself, exported for its known-answer pins. */
+void fa_oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  philox4x32_10(ctr, key, out);
+}
+
+/* Word j & 3 of Philox(counter = (j >> 2, i, bh, offset), key = seed). */
+uint32_t fa_oracle_dropout_word(uint64_t seed, uint32_t offset, int64_t bh, int i, int j) {
+  const uint32_t ctr[4] = {(uint32_t)(j >> 2), (uint32_t)i, (uint32_t)bh, offset};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  philox4x32_10(ctr, key, out);
+  return out[j & 3];
+}
 
 /* ------------------------------------------------------------------ */
 /* a minimal work-sharing loop over items (no arithmetic of the method) */
@@ -119,6 +159,12 @@ typedef struct {
   const uint8_t* bmask;
   int bq, bk, nkb;
   int64_t mstride;
+  /* optional dropout on P: keep (i, j) iff dropout_word >= thr, kept values
+   * scaled by rs = 1 / (1 - p) */
+  int dropout;
+  uint64_t seed;
+  uint32_t offset, thr;
+  double rs;
   /* forward outputs */
   double *o, *lse;
   /* backward-row outputs */
@@ -139,6 +185,12 @@ static double score(const job_t* J, int64_t bh, int i, int j) {
   double acc = 0.0;
   for (int c = 0; c < J->d; ++c) acc += qi[c] * kj[c];
   return J->scale * acc;
+}
+
+/* z_ij * rs: the dropout factor of element (i, j), 1 without dropout. */
+static double drop_factor(const job_t* J, int64_t bh, int i, int j) {
+  if (!J->dropout) return 1.0;
+  return fa_oracle_dropout_word(J->seed, J->offset, bh, i, j) >= J->thr ? J->rs : 0.0;
 }
 
 /* Row i of S and P written out in full (scratch holds 2N doubles):
@@ -174,6 +226,8 @@ static void fwd_item(void* ctx, int64_t it, double* scratch) {
   double m, l;
   softmax_row(J, bh, i, s, p, &m, &l);
   double* oi = J->o + (size_t)it * J->d;
+  if (J->dropout) /* dropout acts on P before P V (lse is unchanged) */
+    for (int j = 0; j < J->N; ++j) p[j] *= drop_factor(J, bh, i, j);
   for (int c = 0; c < J->d; ++c) {
     double acc = 0.0;
     for (int j = 0; j < J->N; ++j)
@@ -183,13 +237,7 @@ static void fwd_item(void* ctx, int64_t it, double* scratch) {
   J->lse[it] = (l > 0.0) ? m + log(l) : -INFINITY;
 }
 
-static void set_mask(job_t* J, const uint8_t* bmask, int bq, int bk, int nkb, int64_t mstride) {
-  J->bmask = bmask;
-  J->bq = bq > 0 ? bq : 1;
-  J->bk = bk > 0 ? bk : 1;
-  J->nkb = nkb;
-  J->mstride = mstride;
-}
+static void set_mask(job_t* J, const uint8_t* bmask, int bq, int bk, int nkb, int64_t mstride);
 
 /* the masked entry points below take the block mask as set by the caller
  * through this thread-local pointer, so the unmasked signatures stay as they
@@ -197,6 +245,22 @@ static void set_mask(job_t* J, const uint8_t* bmask, int bq, int bk, int nkb, in
 static __thread const uint8_t* t_bmask = 0;
 static __thread int t_bq = 1, t_bk = 1, t_nkb = 0;
 static __thread int64_t t_mstride = 0;
+static __thread int t_dropout = 0;
+static __thread uint64_t t_seed = 0;
+static __thread uint32_t t_offset = 0, t_thr = 0;
+static __thread double t_rs = 1.0;
+
+/* Set (enable = 1) or clear dropout for the next calls made by this thread:
+ * element (i, j) of head bh is kept iff fa_oracle_dropout_word(seed, offset,
+ * bh, i, j) >= thr, and kept probabilities are multiplied by rs. */
+void fa_oracle_set_dropout(int enable, uint64_t seed, uint32_t offset, uint32_t thr, double rs) {
+  t_dropout = enable;
+  t_seed = seed;
+  t_offset = offset;
+  t_thr = thr;
+  t_rs = rs;
+}
+
 
 /* Set (or clear with bmask = NULL) the block mask for the next calls made by
  * this thread: bmask[bh * mstride + qb * nkb + kb] != 0 keeps the block of
@@ -207,6 +271,19 @@ void fa_oracle_set_block_mask(const uint8_t* bmask, int bq, int bk, int nkb, int
   t_bk = bk;
   t_nkb = nkb;
   t_mstride = mstride;
+}
+
+static void set_mask(job_t* J, const uint8_t* bmask, int bq, int bk, int nkb, int64_t mstride) {
+  J->bmask = bmask;
+  J->bq = bq > 0 ? bq : 1;
+  J->bk = bk > 0 ? bk : 1;
+  J->nkb = nkb;
+  J->mstride = mstride;
+  J->dropout = t_dropout;
+  J->seed = t_seed;
+  J->offset = t_offset;
+  J->thr = t_thr;
+  J->rs = t_rs;
 }
 
 /* O = P V and lse = m + ln l for the selected rows (all rows when sel is
@@ -237,12 +314,13 @@ static void bwd_row_item(void* ctx, int64_t it, double* scratch) {
   double m, l;
   softmax_row(J, bh, i, s, p, &m, &l);
   const double* dOi = J->dO + ((size_t)bh * N + i) * d;
-  /* dP_ij = sum_c dO_ic v_jc */
+  /* dP_ij = sum_c dO_ic v_jc, times the dropout factor z_ij rs (the
+   * gradient with respect to P of O = (P o Z rs) V) */
   for (int j = 0; j < N; ++j) {
     const double* vj = J->v + ((size_t)bh * N + j) * d;
     double acc = 0.0;
     for (int c = 0; c < d; ++c) acc += dOi[c] * vj[c];
-    dP[j] = acc;
+    dP[j] = acc * drop_factor(J, bh, i, j);
   }
   /* D_i from its definition sum_j P_ij dP_ij ... */
   double D = 0.0;
@@ -251,7 +329,8 @@ static void bwd_row_item(void* ctx, int64_t it, double* scratch) {
   double D_alt = 0.0;
   for (int c = 0; c < d; ++c) {
     double oc = 0.0;
-    for (int j = 0; j < N; ++j) oc += p[j] * J->v[((size_t)bh * N + j) * d + c];
+    for (int j = 0; j < N; ++j)
+      oc += p[j] * drop_factor(J, bh, i, j) * J->v[((size_t)bh * N + j) * d + c];
     D_alt += dOi[c] * oc;
   }
   /* dQ_i = scale * sum_j dS_ij k_j with dS_ij = p_ij (dP_ij - D_i) */
@@ -306,12 +385,14 @@ static void bwd_col_item(void* ctx, int64_t it, double* scratch) {
     const double p = exp(s - J->m_all[ri]) / J->l_all[ri];
     const double* dOi = J->dO + (size_t)ri * d;
     const double* qi = J->q + (size_t)ri * d;
+    const double z = drop_factor(J, bh, i, j);
     double dP = 0.0;
     for (int c = 0; c < d; ++c) dP += dOi[c] * vj[c];
+    dP *= z;
     const double dS = p * (dP - J->D_all[ri]);
     for (int c = 0; c < d; ++c) {
-      dvj[c] += p * dOi[c];  /* dV = P^T dO */
-      dkj[c] += dS * qi[c];  /* dK = scale dS^T Q */
+      dvj[c] += p * z * dOi[c]; /* dV = (P o Z rs)^T dO */
+      dkj[c] += dS * qi[c];     /* dK = scale dS^T Q */
     }
   }
   for (int c = 0; c < d; ++c) dkj[c] *= J->scale;

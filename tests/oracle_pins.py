@@ -15,6 +15,8 @@ import os
 import numpy as np
 import torch
 
+from oracle import dropout_params as oracle_dropout_params
+
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
@@ -454,6 +456,115 @@ def pin_decode(orc):
     _close(lse, scale * np.sum(q[:, 0] * k[:, 0], axis=1), 1e-13, atol=1e-15, what="one-key lse")
 
 
+# ---------------------------------------------------------------- pin 12
+def _read_kat(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, _, val = line.partition("=")
+                vals[key.strip()] = [int(w, 16) for w in val.split()]
+    return vals
+
+
+def _z_scores(count, n, prob):
+    """How many standard deviations a binomial count is from its mean."""
+    return abs(count - n * prob) / math.sqrt(n * prob * (1.0 - prob))
+
+
+def pin_dropout(orc):
+    """Dropout on P (O = (P o Z / (1 - p)) V, lse that of P), with Z replayed
+    from Philox4x32-10.
+
+    The generator against its published known-answer vectors; p = 0 against
+    the plain definition (bit for bit); the keep decisions against their
+    distribution (keep rate, every bit of the word fair, independent across
+    heads, offsets and seeds); the forward against the closed form it has
+    when V is the identity (O is then the dropped, rescaled P); the whole
+    backward against PyTorch fp64 autograd of the same expression given Z;
+    and unbiasedness: averaged over seeds, O tends to the undropped O.
+    """
+    kat = _read_kat("philox4x32_10_kat.txt")
+    for nm in ("zero", "ones", "pi"):
+        got = orc.philox(kat[nm + "_ctr"], kat[nm + "_key"])
+        assert got == kat[nm + "_out"], f"Philox known answer {nm}: {got}"
+
+    rng = _rng(12)
+    BH, N, d, scale = 2, 37, 8, 0.4
+    q, k, v, dO = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    for causal in (False, True):
+        o0, l0 = orc.forward(q, k, v, scale, causal)
+        o1, l1 = orc.forward(q, k, v, scale, causal, dropout=(0.0, 99, 3))
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1), "p = 0 changes O"
+        g0 = orc.backward(q, k, v, dO, scale, causal)
+        g1 = orc.backward(q, k, v, dO, scale, causal, dropout=(0.0, 99, 3))
+        for a, b in zip(g0[:3], g1[:3]):
+            assert np.array_equal(a, b), "p = 0 changes a gradient"
+
+    # keep decisions: rate, fair bits, independence
+    p, seed, off = 0.2, 0x1234_5678_9ABC_DEF0, 7
+    rows, cols = 48, 256
+    words = np.array([[orc.dropout_word(seed, off, 1, i, j) for j in range(cols)]
+                      for i in range(rows)], dtype=np.uint64)
+    n = words.size
+    keep = orc.dropout_keep(p, seed, off, 1, rows, cols)
+    thr = int(np.floor(float(np.float32(p)) * 2**32))
+    assert np.array_equal(keep, words >= thr)
+    assert _z_scores(int(keep.sum()), n, 1.0 - p) < 5.0, "keep rate"
+    for b in range(32):
+        assert _z_scores(int(((words >> b) & 1).sum()), n, 0.5) < 5.0, f"bit {b} biased"
+    for other in ((seed, off, 0), (seed, off + 1, 1), (seed ^ 1, off, 1), (seed ^ 2**40, off, 1)):
+        keep2 = np.array([[orc.dropout_word(other[0], other[1], other[2], i, j) >= thr
+                           for j in range(cols)] for i in range(rows)])
+        agree = int((keep == keep2).sum())
+        assert _z_scores(agree, n, p * p + (1 - p) * (1 - p)) < 5.0, f"not independent {other}"
+
+    # V = identity: O_ij = P_ij Z_ij / (1 - p) exactly
+    Nn = 24
+    qq, kk = rng.standard_normal((2, Nn, Nn)), rng.standard_normal((2, Nn, Nn))
+    eye = np.broadcast_to(np.eye(Nn), (2, Nn, Nn)).copy()
+    P, _ = orc.forward(qq, kk, eye, 0.3, False)
+    pd, seed2, off2 = 0.35, 2024, 5
+    O, _ = orc.forward(qq, kk, eye, 0.3, False, dropout=(pd, seed2, off2))
+    _, rs = oracle_dropout_params(pd)
+    for bh in range(2):
+        Z = orc.dropout_keep(pd, seed2, off2, bh, Nn, Nn)
+        _close(O[bh * Nn:(bh + 1) * Nn], P[bh * Nn:(bh + 1) * Nn] * Z * rs, 1e-15,
+               what="dropout closed form")
+
+    # backward against autograd of the same expression given Z
+    pd, seed3, off3 = 0.25, 77, 1
+    _, rs = oracle_dropout_params(pd)
+    Z = np.stack([orc.dropout_keep(pd, seed3, off3, bh, N, N) for bh in range(BH)])
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        s_ = (tq @ tk.transpose(-1, -2)) * scale
+        if causal:
+            s_ = s_.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), -math.inf)
+        to = (torch.softmax(s_, dim=-1) * torch.tensor(Z, dtype=torch.float64) * rs) @ tv
+        to.backward(torch.tensor(dO))
+        o, lse = orc.forward(q, k, v, scale, causal, dropout=(pd, seed3, off3))
+        _close(o, to.detach().reshape(-1, d).numpy(), 1e-10, atol=1e-12, what="dropout O")
+        _close(lse, torch.logsumexp(s_.detach(), -1).reshape(-1).numpy(), 1e-12, atol=1e-13,
+               what="dropout lse")
+        dq, dk, dv, (_, _, D, D_alt) = orc.backward(q, k, v, dO, scale, causal,
+                                                    dropout=(pd, seed3, off3))
+        _close(D, D_alt, 1e-10, atol=1e-12, what="dropout D forms")
+        for a, t, nm in ((dq, tq, "dQ"), (dk, tk, "dK"), (dv, tv, "dV")):
+            _close(a, t.grad.reshape(-1, d).numpy(), 1e-9, atol=1e-11, what=f"dropout {nm}")
+
+    # unbiased: E[O] over seeds is the undropped O
+    Bs, Ns, ds = 1, 12, 4
+    q4, k4, v4 = (rng.standard_normal((Bs, Ns, ds)) for _ in range(3))
+    ref, _ = orc.forward(q4, k4, v4, 0.5, False)
+    samples = np.stack([orc.forward(q4, k4, v4, 0.5, False, dropout=(0.3, s4, 0), nthreads=1)[0]
+                        for s4 in range(600)])
+    se = samples.std(axis=0) / math.sqrt(samples.shape[0])
+    assert np.all(np.abs(samples.mean(axis=0) - ref) <= 5.0 * se + 1e-12), "dropout biased"
+
+
 ALL_PINS = [pin_worked_example, pin_zero_query, pin_one_hot, pin_permutation,
             pin_online_equals_two_pass, pin_finite_differences, pin_structure,
-            pin_torch_sdpa, pin_selection_consistency, pin_block_mask, pin_decode]
+            pin_torch_sdpa, pin_selection_consistency, pin_block_mask, pin_decode,
+            pin_dropout]

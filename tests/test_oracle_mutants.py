@@ -22,7 +22,7 @@ MUTANTS = [
      "J->lse[it] = (l > 0.0) ? m + log2(l) : -INFINITY;"),
     ("online_beta_dropped", "l = alpha * l + beta * blk_sum;\n    m = m_new;\n    if (m_trace)",
      "l = alpha * l + blk_sum;\n    m = m_new;\n    if (m_trace)"),
-    ("dv_uses_dS", "dvj[c] += p * dOi[c];", "dvj[c] += dS * dOi[c];"),
+    ("dv_uses_dS", "dvj[c] += p * z * dOi[c];", "dvj[c] += dS * z * dOi[c];"),
     ("dk_uses_p", "dkj[c] += dS * qi[c];", "dkj[c] += p * qi[c];"),
     ("no_max_in_p", "for (int j = 0; j < N; ++j) p[j] = exp(s[j] - m) / l;",
      "for (int j = 0; j < N; ++j) p[j] = exp(s[j]) / l;"),
@@ -41,6 +41,18 @@ MUTANTS = [
     ("decode_dot_uses_v", "const double* kj = J->k + ((size_t)bh * Nk + j) * d;",
      "const double* kj = J->v + ((size_t)bh * Nk + j) * d;"),
     ("block_mask_ignores_head", "J->bmask[bh * J->mstride +", "J->bmask[0 * J->mstride +"),
+    ("philox_weyl_constant", "k1 += 0xBB67AE85u;", "k1 += 0x9E3779B9u;"),
+    ("philox_mulhi_swapped", "const uint32_t y0 = (uint32_t)(p1 >> 32) ^ x1 ^ k0;",
+     "const uint32_t y0 = (uint32_t)(p0 >> 32) ^ x1 ^ k0;"),
+    ("dropout_counter_ignores_head", "(uint32_t)i, (uint32_t)bh, offset};",
+     "(uint32_t)i, 0u, offset};"),
+    ("dropout_rescale_dropped", "? J->rs : 0.0;", "? 1.0 : 0.0;"),
+    ("dropout_ij_swapped", "fa_oracle_dropout_word(J->seed, J->offset, bh, i, j) >=",
+     "fa_oracle_dropout_word(J->seed, J->offset, bh, j, i) >="),
+    ("dropout_fwd_ignored", "if (J->dropout) /* dropout acts", "if (0) /* dropout acts"),
+    ("dropout_dv_undropped", "dvj[c] += p * z * dOi[c];", "dvj[c] += p * dOi[c];"),
+    ("dropout_col_dP_undropped", "dP *= z;", "(void)0;"),
+    ("dropout_row_dP_undropped", "dP[j] = acc * drop_factor(J, bh, i, j);", "dP[j] = acc;"),
 ]
 
 
