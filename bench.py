@@ -266,8 +266,8 @@ def run_ours(args, world, rank, local):
     D = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
-    if args.block_mask:
-        return run_sparse(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
+    if args.block_mask or args.dropout:
+        return run_variant(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
     if args.decode:
         return run_decode(args, world, rank, local, fa, w, (q, k, v), stream, dev)
     names = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
@@ -427,29 +427,45 @@ def run_ours(args, world, rank, local):
     return 0
 
 
-def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
-    """Block-sparse step: fa_forward_blocksparse + fa_backward_blocksparse."""
+def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
+    """Block-sparse and / or dropout step: fa_forward_blocksparse +
+    fa_backward_blocksparse (--block-mask), fa_forward_dropout +
+    fa_backward_dropout (--dropout, with the block mask if one is given)."""
     q, k, v, dO = tensors
-    mask_cpu = band_mask(args.block_mask, w.N)
-    mask = mask_cpu.to(dev)
+    if args.block_mask:
+        mask_cpu = band_mask(args.block_mask, w.N)
+        mask = mask_cpu.to(dev)
+    else:
+        mask_cpu = mask = None
+    p_drop = args.dropout or 0.0
+    seed = 0x5EED
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_backward_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
                      device=dev)
 
-    def step(ev=None):
-        fa.fa_forward_blocksparse(q, k, v, mask, causal=causal, scale=w.scale, o=o, lse=lse,
-                                  stream=stream)
+    def step(ev=None, offset=0):
+        if p_drop > 0.0:
+            fa.fa_forward_dropout(q, k, v, p_drop, seed, offset, causal=causal, scale=w.scale,
+                                  block_mask=mask, o=o, lse=lse, stream=stream)
+        else:
+            fa.fa_forward_blocksparse(q, k, v, mask, causal=causal, scale=w.scale, o=o, lse=lse,
+                                      stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_backward_blocksparse(q, k, v, o, dO, lse, mask, causal=causal, scale=w.scale,
-                                   dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        if p_drop > 0.0:
+            fa.fa_backward_dropout(q, k, v, o, dO, lse, p_drop, seed, offset, causal=causal,
+                                   scale=w.scale, block_mask=mask, dq=dq, dk=dk, dv=dv,
+                                   workspace=ws, stream=stream)
+        else:
+            fa.fa_backward_blocksparse(q, k, v, o, dO, lse, mask, causal=causal, scale=w.scale,
+                                       dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(offset=i)
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
@@ -457,7 +473,7 @@ def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     clocks.start()
     for s_ in range(args.steps):
         evs[s_][0].record(stream)
-        step(evs[s_])
+        step(evs[s_], offset=args.warmup + s_)  # a fresh dropout mask every step
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
@@ -467,7 +483,10 @@ def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     ms = max_over_ranks(fwd_ms + bwd_ms, world)
-    E = kept_elements(mask_cpu, w.N, causal) * w.B * w.H
+    if mask_cpu is not None:
+        E = kept_elements(mask_cpu, w.N, causal) * w.B * w.H
+    else:
+        E = w.B * w.H * w.N * w.N * (0.5 if causal else 1.0)
     f_fwd, f_bwd = 4.0 * w.d * E, 10.0 * w.d * E
     peaks, peak_src = read_peaks()
     peak = peaks["bf16_tflops"]
@@ -475,9 +494,14 @@ def run_sparse(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     if rank == 0:
         dense = w.B * w.H * w.N * w.N * (0.5 if causal else 1.0)
         cfg = workload_config(w, causal)
-        cfg.update({"block_mask": args.block_mask, "kept_fraction": E / dense})
+        if mask_cpu is not None:
+            cfg.update({"block_mask": args.block_mask, "kept_fraction": E / dense})
+        if p_drop > 0.0:
+            cfg.update({"dropout_p": p_drop, "dropout_rng": "Philox4x32-10, new offset per step"})
+        what = ", ".join(x for x in ("block-sparse, FLOPs of kept tiles" if mask_cpu is not None
+                                     else "", f"dropout p={p_drop}" if p_drop > 0 else "") if x)
         line = {
-            "metric": METRIC + " (block-sparse, FLOPs of kept tiles)",
+            "metric": METRIC + f" ({what})",
             "value": world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -561,6 +585,8 @@ def main():
     ap.add_argument("--causal", type=int, default=None, help="override the workload's mask mode")
     ap.add_argument("--block-mask", default=None,
                     help="time the block-sparse path with mask band:W[:G] (tiles of 128)")
+    ap.add_argument("--dropout", type=float, default=None,
+                    help="time the dropout path with this probability (0 < p < 1)")
     ap.add_argument("--decode", type=int, default=None,
                     help="time the decode step with this many query rows (<= 16)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -60,6 +60,13 @@ def library():
         lib.fa_backward_blocksparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
                                                 i, vp, ll, vp, sz, vp]
         lib.fa_backward_blocksparse.restype = i
+        u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
+        lib.fa_forward_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u32, vp,
+                                           ll, vp]
+        lib.fa_forward_dropout.restype = i
+        lib.fa_backward_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i,
+                                            f, u64, u32, vp, ll, vp, sz, vp]
+        lib.fa_backward_dropout.restype = i
         lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -187,6 +194,60 @@ def fa_backward_blocksparse(q, k, v, o, dO, lse, block_mask, causal: bool = Fals
                                            ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_blocksparse")
+    return dq, dk, dv
+
+
+def fa_forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0,
+                       causal: bool = False, scale: float | None = None, block_mask=None,
+                       o=None, lse=None, stream=None):
+    """O = (softmax(scale q k^T) o Z / (1 - p_drop)) v and the lse of the
+    undropped softmax; Z is replayed from Philox4x32-10 at (seed, offset).
+    block_mask: None (dense) or a uint8 CUDA block mask as for
+    fa_forward_blocksparse."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    mp, ms = (None, 0) if block_mask is None else _mask_args(block_mask, B, H, N)
+    st = library().fa_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                      float(scale), int(bool(causal)), float(p_drop),
+                                      int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp, ms,
+                                      ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward_dropout")
+    return o, lse
+
+
+def fa_backward_dropout(q, k, v, o, dO, lse, p_drop: float, seed: int, offset: int = 0,
+                        causal: bool = False, scale: float | None = None, block_mask=None,
+                        dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """(dq, dk, dv) of fa_forward_dropout with the same p_drop, seed, offset."""
+    B, H, N, d = q.shape
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    need = fa_backward_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    mp, ms = (None, 0) if block_mask is None else _mask_args(block_mask, B, H, N)
+    st = library().fa_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                       int(bool(causal)), float(p_drop),
+                                       int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp, ms,
+                                       _ptr(workspace), workspace.numel(),
+                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_backward_dropout")
     return dq, dk, dv
 
 

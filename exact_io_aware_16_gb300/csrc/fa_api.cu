@@ -87,7 +87,7 @@ const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "ok";
     case FA_ERR_NULL: return "null pointer";
-    case FA_ERR_SHAPE: return "invalid shape or scale";
+    case FA_ERR_SHAPE: return "invalid shape, scale or dropout probability";
     case FA_ERR_HEADDIM: return "head dimension must be 64 or 128";
     case FA_ERR_ALIGN: return "pointer not 16-byte aligned";
     case FA_ERR_ARCH: return "device is not sm_103 (GB300)";
@@ -108,7 +108,7 @@ long long fa_forward_tile_count(int N, int causal) {
 
 static int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int N, int d, float scale, int causal, const uint8_t* bmask,
-                        long long mstride, void* stream) {
+                        long long mstride, void* stream, const fa::DropArgs* drop = nullptr) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
@@ -135,6 +135,10 @@ static int forward_impl(const void* q, const void* k, const void* v, void* o, fl
   a.causal = causal ? 1 : 0;
   a.bmask = bmask;
   a.mstride = mstride;
+  if (drop) {
+    a.dropout = true;
+    a.drop = *drop;
+  }
   cudaError_t e = fa::launch_forward(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -181,7 +185,8 @@ int fa_backward_preprocess(const void* o, const void* dO, float* D, int B, int H
 static int bwd_step(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                     float* D, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                     float scale, int causal, void* stream, bool do_dkdv, bool do_dq,
-                    const uint8_t* bmask = nullptr, long long mstride = 0) {
+                    const uint8_t* bmask = nullptr, long long mstride = 0,
+                    const fa::DropArgs* drop = nullptr) {
   if (!q || !k || !v || !dO || !lse || !D) return FA_ERR_NULL;
   if ((do_dkdv && (!dk || !dv)) || (do_dq && !dq)) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
@@ -216,6 +221,10 @@ static int bwd_step(const void* q, const void* k, const void* v, const void* dO,
   a.causal = causal ? 1 : 0;
   a.bmask = bmask;
   a.mstride = mstride;
+  if (drop) {
+    a.dropout = true;
+    a.drop = *drop;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // dQ first: it refines D in place (exact D = sum_j P_ij dP_ij), which the
   // dK / dV kernel then reads.
@@ -242,7 +251,7 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                          int H, int N, int d, float scale, int causal, const uint8_t* bmask,
                          long long mstride, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, const fa::DropArgs* drop = nullptr) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
@@ -257,7 +266,7 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
   float* D = static_cast<float*>(workspace);
   if ((st = fa_backward_preprocess(o, dO, D, B, H, N, d, stream)) != FA_OK) return st;
   return bwd_step(q, k, v, dO, lse, D, dq, dk, dv, B, H, N, d, scale, causal, stream, true, true,
-                  bmask, mstride);
+                  bmask, mstride, drop);
 }
 
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -276,6 +285,49 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
   if (st != FA_OK) return st;
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, block_mask,
                        mask_head_stride, workspace, workspace_bytes, stream);
+}
+
+// Dropout parameters of probability p: keep iff the generator's word is
+// >= floor(p * 2^32), kept values times 1 / (1 - p).  p must lie in [0, 1);
+// p = 0 keeps everything and runs the kernels without dropout (returns false).
+static int make_drop(float p, unsigned long long seed, unsigned int offset, fa::DropArgs* out,
+                     bool* active) {
+  if (!(p >= 0.0f && p < 1.0f)) return FA_ERR_SHAPE;  // also rejects NaN
+  *active = p > 0.0f;
+  out->set_seed(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  out->offset = offset;
+  out->thr = static_cast<uint32_t>(static_cast<double>(p) * 4294967296.0);  // floor, < 2^32
+  out->rs = 1.0f / (1.0f - p);
+  return FA_OK;
+}
+
+int fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, int causal, float p_drop,
+                       unsigned long long seed, unsigned int offset, const uint8_t* block_mask,
+                       long long mask_head_stride, void* stream) {
+  fa::DropArgs dr;
+  bool active = false;
+  int st = make_drop(p_drop, seed, offset, &dr, &active);
+  if (st != FA_OK) return st;
+  if (block_mask && (st = check_sparse(block_mask, mask_head_stride, N)) != FA_OK) return st;
+  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask,
+                      block_mask ? mask_head_stride : 0, stream, active ? &dr : nullptr);
+}
+
+int fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, float scale, int causal, float p_drop,
+                        unsigned long long seed, unsigned int offset, const uint8_t* block_mask,
+                        long long mask_head_stride, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  fa::DropArgs dr;
+  bool active = false;
+  int st = make_drop(p_drop, seed, offset, &dr, &active);
+  if (st != FA_OK) return st;
+  if (block_mask && (st = check_sparse(block_mask, mask_head_stride, N)) != FA_OK) return st;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, block_mask,
+                       block_mask ? mask_head_stride : 0, workspace, workspace_bytes, stream,
+                       active ? &dr : nullptr);
 }
 
 static int check_decode_shape(int B, int H, int Nq, int Nk, int d) {

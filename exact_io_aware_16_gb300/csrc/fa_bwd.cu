@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -303,7 +304,13 @@ __device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bf
 // ============================================================ dK / dV
 // SPARSE: only the query tiles whose block-mask entry for this key tile is
 // set are visited (a compact list built by warp 0).
-template <int D, bool CAUSAL, bool SPARSE>
+//
+// DROPOUT (dropout on P with keep matrix Z and factor rs = 1 / (1 - p)):
+// dV = rs (P o Z)^T dO and dS = P o (rs Z o dP - D); P itself (undropped)
+// stays in registers for dS, P o Z goes to the dV product, rs is applied when
+// dV is stored.  The keep bits of a key row come transposed from the
+// generator's row-major counters (keep_nibble_t).
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq,
                        const __grid_constant__ CUtensorMap tk,
@@ -311,7 +318,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
                        const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
-                       float scale_log2, const uint8_t* __restrict__ bmask, long long mstride) {
+                       float scale_log2, const uint8_t* __restrict__ bmask, long long mstride,
+                       DropArgs drop) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -427,6 +435,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // lse * log2(e) and D of this query tile, staged with the tiles
       const float* lse2_s = vec + (n % kStages) * 256;
       const float* D_s = lse2_s + 128;
+      // dropout keep bits of this key row for query rows q0 + col0 + c (bit c
+      // of kb[c / 32]), drawn before the scores are waited for
+      uint32_t kb[2] = {0u, 0u};
+      if (DROPOUT) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          kb[u >> 3] |= keep_nibble_t(drop, static_cast<uint32_t>(krow),
+                                      static_cast<uint32_t>(q0) + col0 + 4u * u,
+                                      static_cast<uint32_t>(bh), lane)
+                        << (4 * (u & 7));
+        reg_pin(kb);  // drawn here, before the wait, not next to their use
+      }
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x301)) {
         ok = false;
         break;
@@ -452,8 +472,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = __uint_as_float(pr[2 * c]), p1 = __uint_as_float(pr[2 * c + 1]);
+          if (DROPOUT) {  // P o Z for the dV product
+            const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
+            pk[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+          } else {
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+        }
         tmem_st32(tmem + lane_off + L::kSCol + col0, pk);
       }
       tmem_st_wait();
@@ -477,10 +504,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 dd = d4[e4];
           const int c = c2 * 32 + 4 * e4;
-          const float ds0 = __uint_as_float(pr[c]) * (__uint_as_float(r[4 * e4]) - dd.x);
-          const float ds1 = __uint_as_float(pr[c + 1]) * (__uint_as_float(r[4 * e4 + 1]) - dd.y);
-          const float ds2 = __uint_as_float(pr[c + 2]) * (__uint_as_float(r[4 * e4 + 2]) - dd.z);
-          const float ds3 = __uint_as_float(pr[c + 3]) * (__uint_as_float(r[4 * e4 + 3]) - dd.w);
+          float dp[4] = {__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1]),
+                         __uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])};
+          if (DROPOUT) {  // dP of the dropped product: rs Z o (dO V^T)
+            const uint32_t bits = kb[c >> 5] >> (c & 31);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dp[e] = ((bits >> e) & 1u) ? dp[e] * drop.rs : 0.0f;
+          }
+          const float ds0 = __uint_as_float(pr[c]) * (dp[0] - dd.x);
+          const float ds1 = __uint_as_float(pr[c + 1]) * (dp[1] - dd.y);
+          const float ds2 = __uint_as_float(pr[c + 2]) * (dp[2] - dd.z);
+          const float ds3 = __uint_as_float(pr[c + 3]) * (dp[3] - dd.w);
           w[2 * e4] = pack_bf16x2(ds0, ds1);
           w[2 * e4 + 1] = pack_bf16x2(ds2, ds3);
         }
@@ -508,11 +542,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const size_t off = (static_cast<size_t>(bh) * N + (valid ? krow : 0)) * D;
       // d = 128: warpgroup g stores columns [64g, 64g+64) of dV and dK;
       // d = 64: warpgroup 0 stores dV, warpgroup 1 stores dK
+      const float dv_mul = DROPOUT ? drop.rs : 1.0f;
       if (D == 128) {
-        store_acc_half(tmem + lane_off + L::kAcc0 + col0, 1.0f, dv + off + col0, valid);
+        store_acc_half(tmem + lane_off + L::kAcc0 + col0, dv_mul, dv + off + col0, valid);
         store_acc_half(tmem + lane_off + L::kAcc1 + col0, scale, dk + off + col0, valid);
       } else if (g == 0) {
-        store_acc_half(tmem + lane_off + L::kAcc0, 1.0f, dv + off, valid);
+        store_acc_half(tmem + lane_off + L::kAcc0, dv_mul, dv + off, valid);
       } else {
         store_acc_half(tmem + lane_off + L::kAcc1, scale, dk + off, valid);
       }
@@ -531,14 +566,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // D~_i for the dK/dV kernel that runs next.
 // SPARSE: only the key tiles this query tile keeps in the block mask are
 // visited (a compact list built by warp 0).
-template <int D, bool CAUSAL, bool SPARSE>
+//
+// DROPOUT: dP becomes rs Z o (dO V^T) (the exact D and dS use it); B = P K
+// keeps the undropped P, since dS = P o (dP - D) is linear in D.
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv,
                      const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
                      float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
                      float scale, float scale_log2, const uint8_t* __restrict__ bmask,
-                     long long mstride) {
+                     long long mstride, DropArgs drop) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -651,6 +689,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float dxp[4] = {0.f, 0.f, 0.f, 0.f};  // this half's part of the exact D = sum_j P_ij dP_ij
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
+      // dropout keep bits of this row for keys kt_of(n) * 128 + col0 + c
+      // (bit c of kb[c / 32]), drawn before the scores are waited for
+      uint32_t kb[2] = {0u, 0u};
+      if (DROPOUT) {
+        const uint32_t jg0 = (static_cast<uint32_t>(kt_of(n)) * 128u + col0) >> 2;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          kb[u >> 3] |= keep_nibble(drop, jg0 + u, static_cast<uint32_t>(row),
+                                    static_cast<uint32_t>(bh)) << (4 * (u & 7));
+        reg_pin(kb);  // drawn here, before the wait, not next to their use
+      }
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {
         ok = false;
         break;
@@ -695,7 +744,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 16; ++e) {
           const int c = c2 * 32 + 2 * e;
           const float p0 = __uint_as_float(pr[c]), p1 = __uint_as_float(pr[c + 1]);
-          const float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
+          float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
+          if (DROPOUT) {  // dP of the dropped product: rs Z o (dO V^T)
+            const uint32_t bits = kb[c >> 5] >> (c & 31);
+            dp0 = (bits & 1u) ? dp0 * drop.rs : 0.0f;
+            dp1 = (bits & 2u) ? dp1 * drop.rs : 0.0f;
+          }
           dxp[(2 * e) & 3] = fmaf(p0, dp0, dxp[(2 * e) & 3]);
           dxp[(2 * e + 1) & 3] = fmaf(p1, dp1, dxp[(2 * e + 1) & 3]);
           w[e] = pack_bf16x2(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
@@ -768,9 +822,9 @@ cudaError_t prep(Kern k, uint32_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int D, bool CAUSAL, bool SPARSE>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, SPARSE>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, SPARSE, DROPOUT>;
   constexpr uint32_t smem = BwdLayout<D>::kSmem;
   cudaError_t e = prep(kern, smem);
   if (e != cudaSuccess) return e;
@@ -778,13 +832,14 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
-      static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride);
+      static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride,
+      a.drop);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool SPARSE>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL, SPARSE>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, SPARSE, DROPOUT>;
   constexpr uint32_t smem = BwdLayout<D>::kSmem;
   cudaError_t e = prep(kern, smem);
   if (e != cudaSuccess) return e;
@@ -792,22 +847,26 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.BH, a.N,
-      a.scale, a.scale_log2, a.bmask, a.mstride);
+      a.scale, a.scale_log2, a.bmask, a.mstride, a.drop);
   return cudaGetLastError();
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool DROPOUT>
 cudaError_t launch_dkdv_s(const BwdArgs& a, cudaStream_t s) {
   if (a.d == 64)
-    return a.causal ? launch_dkdv_t<64, true, SPARSE>(a, s) : launch_dkdv_t<64, false, SPARSE>(a, s);
-  return a.causal ? launch_dkdv_t<128, true, SPARSE>(a, s) : launch_dkdv_t<128, false, SPARSE>(a, s);
+    return a.causal ? launch_dkdv_t<64, true, SPARSE, DROPOUT>(a, s)
+                    : launch_dkdv_t<64, false, SPARSE, DROPOUT>(a, s);
+  return a.causal ? launch_dkdv_t<128, true, SPARSE, DROPOUT>(a, s)
+                  : launch_dkdv_t<128, false, SPARSE, DROPOUT>(a, s);
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool DROPOUT>
 cudaError_t launch_dq_s(const BwdArgs& a, cudaStream_t s) {
   if (a.d == 64)
-    return a.causal ? launch_dq_t<64, true, SPARSE>(a, s) : launch_dq_t<64, false, SPARSE>(a, s);
-  return a.causal ? launch_dq_t<128, true, SPARSE>(a, s) : launch_dq_t<128, false, SPARSE>(a, s);
+    return a.causal ? launch_dq_t<64, true, SPARSE, DROPOUT>(a, s)
+                    : launch_dq_t<64, false, SPARSE, DROPOUT>(a, s);
+  return a.causal ? launch_dq_t<128, true, SPARSE, DROPOUT>(a, s)
+                  : launch_dq_t<128, false, SPARSE, DROPOUT>(a, s);
 }
 
 }  // namespace
@@ -827,11 +886,15 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long 
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
-  return a.bmask ? launch_dkdv_s<true>(a, s) : launch_dkdv_s<false>(a, s);
+  if (a.dropout)
+    return a.bmask ? launch_dkdv_s<true, true>(a, s) : launch_dkdv_s<false, true>(a, s);
+  return a.bmask ? launch_dkdv_s<true, false>(a, s) : launch_dkdv_s<false, false>(a, s);
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  return a.bmask ? launch_dq_s<true>(a, s) : launch_dq_s<false>(a, s);
+  if (a.dropout)
+    return a.bmask ? launch_dq_s<true, true>(a, s) : launch_dq_s<false, true>(a, s);
+  return a.bmask ? launch_dq_s<true, false>(a, s) : launch_dq_s<false, false>(a, s);
 }
 
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s) {

@@ -24,6 +24,12 @@
 //   * causal masking ("FlashAttention ..." talk, optional masking): query
 //     tile i visits key tiles 0..i only; the mask is applied inside the
 //     diagonal tile, so whole tiles above the diagonal are never loaded.
+//   * dropout (the talk's dropout on P, fused with the softmax): with
+//     DROPOUT each thread draws the keep bits of its row for the next key
+//     tile from Philox4x32-10 (philox.cuh) while the tensor core computes the
+//     scores, zeroes dropped entries of P~ before the P V product (the row
+//     sum l keeps them: lse is that of P), and scales O by 1 / (1 - p) at
+//     the end.
 //
 // Ping-pong schedule of the MMA warp for key tile j:
 //     PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
@@ -40,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -99,12 +106,12 @@ __device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity, FwdBars
 // (entry = key tile | keep-by-tile-0 << 14 | keep-by-tile-1 << 15); for each
 // list entry both query tiles compute their scores, and a query tile that
 // does not keep the key tile masks all of it to -inf.
-template <int D, bool CAUSAL, bool SPARSE>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int BH, int N, float scale_log2,
-                  const uint8_t* __restrict__ bmask, long long mstride) {
+                  const uint8_t* __restrict__ bmask, long long mstride, DropArgs drop) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -299,6 +306,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
+      // dropout keep bits of this row for the 128 keys of the tile (bit c of
+      // kb[c / 32] for key kv0 + c), drawn before the scores are waited for
+      uint32_t kb[4] = {0u, 0u, 0u, 0u};
+      if (DROPOUT) {
+        const uint32_t jg0 = static_cast<uint32_t>(kv_of(j) * kTileN) >> 2;
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          kb[u >> 3] |= keep_nibble(drop, jg0 + u, static_cast<uint32_t>(row),
+                                    static_cast<uint32_t>(bh)) << (4 * (u & 7));
+        reg_pin(kb);  // drawn here, before the wait, not next to their use
+      }
       if (!warp_wait(&bars->s_full[g], j & 1, bars, 0x301)) {
         ok = false;
         break;
@@ -351,7 +369,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
         sp[c & 7] += p0 + p1;
-        sr[c] = pack_bf16x2(p0, p1);
+        if (DROPOUT) {
+          const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
+          sr[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+        } else {
+          sr[c] = pack_bf16x2(p0, p1);
+        }
       }
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -386,8 +409,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     } else if (ok && warp_wait(&bars->pv_done[g], (nkv - 1) & 1, bars, 0x303)) {
       tc_fence_after_sync();
-      // a row with no visible key (block-sparse) has l = 0: O = 0, lse = -inf
-      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      // a row with no visible key (block-sparse) has l = 0: O = 0, lse = -inf;
+      // with dropout the kept terms carry the factor 1 / (1 - p)
+      const float inv_l = l_run > 0.0f ? (DROPOUT ? drop.rs : 1.0f) / l_run : 0.0f;
       __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -431,9 +455,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool SPARSE>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE, DROPOUT>;
   constexpr uint32_t smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -442,21 +466,25 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
-      a.bmask, a.mstride);
+      a.bmask, a.mstride, a.drop);
   return cudaGetLastError();
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool DROPOUT>
 cudaError_t launch_forward_s(const FwdArgs& a, cudaStream_t s) {
   if (a.d == 64)
-    return a.causal ? launch_fwd_t<64, true, SPARSE>(a, s) : launch_fwd_t<64, false, SPARSE>(a, s);
-  return a.causal ? launch_fwd_t<128, true, SPARSE>(a, s) : launch_fwd_t<128, false, SPARSE>(a, s);
+    return a.causal ? launch_fwd_t<64, true, SPARSE, DROPOUT>(a, s)
+                    : launch_fwd_t<64, false, SPARSE, DROPOUT>(a, s);
+  return a.causal ? launch_fwd_t<128, true, SPARSE, DROPOUT>(a, s)
+                  : launch_fwd_t<128, false, SPARSE, DROPOUT>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
-  return a.bmask ? launch_forward_s<true>(a, s) : launch_forward_s<false>(a, s);
+  if (a.dropout)
+    return a.bmask ? launch_forward_s<true, true>(a, s) : launch_forward_s<false, true>(a, s);
+  return a.bmask ? launch_forward_s<true, false>(a, s) : launch_forward_s<false, false>(a, s);
 }
 
 cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s) {

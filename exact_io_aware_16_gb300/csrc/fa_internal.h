@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "philox.cuh"
+
 namespace fa {
 
 constexpr int kTileM = 128;   // query rows per tile
@@ -33,6 +35,8 @@ struct FwdArgs {
   int causal;
   const uint8_t* bmask = nullptr;  // block-sparse mask (nullptr: dense)
   long long mstride = 0;           // elements between (b,h) masks (0: one shared mask)
+  bool dropout = false;            // dropout on P with the parameters in drop
+  DropArgs drop;
 };
 
 struct BwdArgs {
@@ -51,6 +55,8 @@ struct BwdArgs {
   int causal;
   const uint8_t* bmask = nullptr;  // block-sparse mask (nullptr: dense)
   long long mstride = 0;
+  bool dropout = false;  // dropout on P with the parameters in drop
+  DropArgs drop;
 };
 
 struct DecodeArgs {

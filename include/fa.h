@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_NULL = -1,           /* a required pointer is NULL */
-  FA_ERR_SHAPE = -2,          /* B, H or N < 1, sizes overflow, or bad scale */
+  FA_ERR_SHAPE = -2,          /* B, H or N < 1, sizes overflow, bad scale or p_drop */
   FA_ERR_HEADDIM = -3,        /* d not in {64, 128} */
   FA_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned */
   FA_ERR_ARCH = -5,           /* current device is not sm_103 */
@@ -172,6 +172,37 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
                             int B, int H, int N, int d, float scale, int causal,
                             const uint8_t* block_mask, long long mask_head_stride,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Attention with dropout on the probabilities (the talk's dropout applied to
+ * P before the product with V, fused with the softmax so P never reaches
+ * memory):  O = (P o Z / (1 - p_drop)) V, with P = softmax(scale Q K^T) and
+ * lse that of P (before dropout).
+ *  - Z is replayed, never stored: element (i, j) of head bh = b*H + h is kept
+ *    iff word j % 4 of Philox4x32-10 (Salmon et al., "Parallel random
+ *    numbers: as easy as 1, 2, 3", SC 2011) at counter
+ *    (j / 4, i, bh, offset) with key (seed & 0xffffffff, seed >> 32) is
+ *    >= floor(p_drop * 2^32).  The backward must get the same p_drop, seed
+ *    and offset as the forward; callers advance offset (or the seed) between
+ *    independent draws.
+ *  - 0 <= p_drop < 1, else FA_ERR_SHAPE.  p_drop = 0 runs the kernels of
+ *    fa_forward / fa_backward (identical results).
+ *  - block_mask: NULL for dense attention, else a block mask as for
+ *    fa_forward_blocksparse (with its limits); dropout applies on top.
+ *  - The backward gives the gradients of that O: dv = (P o Z)^T dO / (1 - p),
+ *    dP = (dO V^T) o Z / (1 - p), dS = P o (dP - D), dq, dk as usual.
+ * All other arguments, layouts and errors as for fa_forward / fa_backward.
+ */
+int fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, int causal, float p_drop,
+                       unsigned long long seed, unsigned int offset, const uint8_t* block_mask,
+                       long long mask_head_stride, void* stream);
+int fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, float scale, int causal, float p_drop,
+                        unsigned long long seed, unsigned int offset, const uint8_t* block_mask,
+                        long long mask_head_stride, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /*
  * Decode step: Nq new query rows against an Nk-row key/value cache (the KV

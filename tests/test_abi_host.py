@@ -98,6 +98,28 @@ def test_blocksparse_validation(lib):
              None, 0, FAKE * 16, 1 << 20, None) == -1
 
 
+def test_dropout_validation(lib):
+    f = lib.fa_forward_dropout
+    g = lib.fa_backward_dropout
+
+    def fw(p=0.1, q=FAKE, mask=None, stride=0, N=256):
+        return f(q, FAKE, FAKE, FAKE, FAKE, 1, 1, N, 64, 0.125, 0, p, 7, 0, mask, stride, None)
+
+    for p in (-0.01, 1.0, 2.0, float("nan"), float("inf")):
+        assert fw(p=p) == -2
+    assert fw(q=None) == -1
+    assert fw(mask=FAKE, stride=-1) == -2
+    assert fw(mask=FAKE, N=128 * 1024 + 1) == -2
+
+    def bw(p=0.1, q=FAKE, w=FAKE * 16):
+        return g(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 0.125, 0, p,
+                 7, 0, None, 0, w, 1 << 20, None)
+
+    assert bw(p=1.5) == -2
+    assert bw(q=None) == -1
+    assert bw(w=None) == -6
+
+
 def test_decode_validation(lib):
     ws = lib.fa_decode_workspace_size(2, 4, 8, 1000, 128)
     assert ws > 0 and ws % 256 == 0
