@@ -29,8 +29,9 @@ What each function follows:
 * ``dropout=(p, seed, offset)`` (the talk's dropout on P before the product
   with V, transcript Q&A after 10:00): O = (P o Z / (1 - p)) V, lse that of
   P.  Z is drawn by Philox4x32-10 (Salmon et al., SC 2011) at counter
-  (j // 4, i, bh, offset) with key seed, word j % 4; an element is kept iff
-  that word is >= floor(p * 2^32).
+  (j // 8, i, bh, offset) with key seed: key j takes the low (even j) or
+  high (odd j) 16 bits of word (j // 2) % 4, and is kept iff they are
+  >= floor(p * 2^16); kept values are scaled by the inverse keep probability.
 
 Parity of every function here is pinned in ``tests/test_oracle_pins.py``.
 """
@@ -134,8 +135,8 @@ class Oracle:
         lib.fa_oracle_set_dropout.argtypes = [i, ctypes.c_uint64, ctypes.c_uint32,
                                               ctypes.c_uint32, d]
         lib.fa_oracle_set_dropout.restype = None
-        lib.fa_oracle_dropout_word.argtypes = [ctypes.c_uint64, ctypes.c_uint32, i64, i, i]
-        lib.fa_oracle_dropout_word.restype = ctypes.c_uint32
+        lib.fa_oracle_dropout_u16.argtypes = [ctypes.c_uint64, ctypes.c_uint32, i64, i, i]
+        lib.fa_oracle_dropout_u16.restype = ctypes.c_uint32
         lib.fa_oracle_philox4x32_10.argtypes = [ctypes.c_void_p] * 3
         lib.fa_oracle_philox4x32_10.restype = None
         for f in (lib.fa_oracle_forward, lib.fa_oracle_backward_rows,
@@ -292,11 +293,11 @@ class Oracle:
         self.lib.fa_oracle_philox4x32_10(c.ctypes.data, kk.ctypes.data, out.ctypes.data)
         return [int(x) for x in out]
 
-    def dropout_word(self, seed: int, offset: int, bh: int, i: int, j: int) -> int:
-        """The 32-bit uniform word that decides element (i, j) of head bh."""
-        return int(self.lib.fa_oracle_dropout_word(int(seed) & (2**64 - 1),
-                                                   int(offset) & 0xFFFFFFFF, int(bh),
-                                                   int(i), int(j)))
+    def dropout_u16(self, seed: int, offset: int, bh: int, i: int, j: int) -> int:
+        """The 16-bit uniform that decides element (i, j) of head bh."""
+        return int(self.lib.fa_oracle_dropout_u16(int(seed) & (2**64 - 1),
+                                                  int(offset) & 0xFFFFFFFF, int(bh),
+                                                  int(i), int(j)))
 
     def dropout_keep(self, p: float, seed: int, offset: int, bh: int, n_rows: int, n_cols: int):
         """Keep matrix Z [n_rows, n_cols] (bool) of head bh."""
@@ -304,7 +305,7 @@ class Oracle:
         z = np.empty((n_rows, n_cols), dtype=bool)
         for i in range(n_rows):
             for j in range(n_cols):
-                z[i, j] = self.dropout_word(seed, offset, bh, i, j) >= thr
+                z[i, j] = self.dropout_u16(seed, offset, bh, i, j) >= thr
         return z
 
     def online_softmax(self, x, block: int):
@@ -338,13 +339,15 @@ def dropout_params(p: float):
     """(thr, rs) of a dropout probability p in [0, 1).
 
     p is first rounded to IEEE single (the precision the library takes it
-    in); an element is kept iff its 32-bit word is >= thr = floor(p * 2^32),
-    and kept values are scaled by rs = 1 / (1 - p).
+    in); an element is kept iff its 16-bit uniform is >= thr = floor(p * 2^16),
+    so it is kept with probability (65536 - thr) / 65536, and kept values are
+    scaled by the inverse of that, rs = 65536 / (65536 - thr).
     """
     p32 = float(np.float32(p))
     if not 0.0 <= p32 < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
-    return int(np.floor(p32 * 4294967296.0)), 1.0 / (1.0 - p32)
+    thr = int(np.floor(p32 * 65536.0))
+    return thr, 65536.0 / (65536.0 - thr)
 
 
 def default() -> Oracle:
@@ -384,8 +387,8 @@ def online_attention_row(*a, **kw):
     return default().online_attention_row(*a, **kw)
 
 
-def dropout_word(*a, **kw):
-    return default().dropout_word(*a, **kw)
+def dropout_u16(*a, **kw):
+    return default().dropout_u16(*a, **kw)
 
 
 def dropout_keep(*a, **kw):

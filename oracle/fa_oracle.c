@@ -38,9 +38,11 @@
  *    the kept blocks.  A row with no visible key has no softmax; it is defined
  *    here as o = 0, lse = -inf and zero gradients.
  *  - dropout (the talk: dropout applied to P before the product with V):
- *    O = (P o Z / (1 - p)) V with Z_ij in {0, 1} drawn by the counter-based
+ *    O = (P o Z / q) V with Z_ij in {0, 1} drawn by the counter-based
  *    Philox4x32-10 generator (see philox4x32_10), so the same Z can be
- *    replayed exactly; lse is that of P (before dropout).
+ *    replayed exactly, and q the keep probability; lse is that of P (before
+ *    dropout).  Each decision uses 16 random bits: p is taken as the
+ *    multiple thr / 65536 of 2^-16 below it, q = 1 - thr / 65536.
  *
  * Layout: every [BH][N][d] array is row-major with index (bh*N + i)*d + c.
  * Row / column selections are flat indices r = bh*N + i.
@@ -79,13 +81,17 @@ void fa_oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint3
   philox4x32_10(ctr, key, out);
 }
 
-/* Word j & 3 of Philox(counter = (j >> 2, i, bh, offset), key = seed). */
-uint32_t fa_oracle_dropout_word(uint64_t seed, uint32_t offset, int64_t bh, int i, int j) {
-  const uint32_t ctr[4] = {(uint32_t)(j >> 2), (uint32_t)i, (uint32_t)bh, offset};
+/* The 16-bit uniform that decides element (i, j) of head bh: one Philox
+ * call (counter = (j / 8, i, bh, offset), key = seed) serves eight
+ * consecutive keys; key j takes word (j / 2) % 4 of it, its low half for
+ * even j and its high half for odd j. */
+uint32_t fa_oracle_dropout_u16(uint64_t seed, uint32_t offset, int64_t bh, int i, int j) {
+  const uint32_t ctr[4] = {(uint32_t)(j / 8), (uint32_t)i, (uint32_t)bh, offset};
   const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
   uint32_t out[4];
   philox4x32_10(ctr, key, out);
-  return out[j & 3];
+  const uint32_t word = out[(j / 2) % 4];
+  return (j % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);
 }
 
 /* ------------------------------------------------------------------ */
@@ -159,8 +165,9 @@ typedef struct {
   const uint8_t* bmask;
   int bq, bk, nkb;
   int64_t mstride;
-  /* optional dropout on P: keep (i, j) iff dropout_word >= thr, kept values
-   * scaled by rs = 1 / (1 - p) */
+  /* optional dropout on P: keep (i, j) iff its 16-bit uniform >= thr, kept
+   * values scaled by rs = 65536 / (65536 - thr), the inverse of the keep
+   * probability */
   int dropout;
   uint64_t seed;
   uint32_t offset, thr;
@@ -190,7 +197,7 @@ static double score(const job_t* J, int64_t bh, int i, int j) {
 /* z_ij * rs: the dropout factor of element (i, j), 1 without dropout. */
 static double drop_factor(const job_t* J, int64_t bh, int i, int j) {
   if (!J->dropout) return 1.0;
-  return fa_oracle_dropout_word(J->seed, J->offset, bh, i, j) >= J->thr ? J->rs : 0.0;
+  return fa_oracle_dropout_u16(J->seed, J->offset, bh, i, j) >= J->thr ? J->rs : 0.0;
 }
 
 /* Row i of S and P written out in full (scratch holds 2N doubles):
@@ -251,7 +258,7 @@ static __thread uint32_t t_offset = 0, t_thr = 0;
 static __thread double t_rs = 1.0;
 
 /* Set (enable = 1) or clear dropout for the next calls made by this thread:
- * element (i, j) of head bh is kept iff fa_oracle_dropout_word(seed, offset,
+ * element (i, j) of head bh is kept iff fa_oracle_dropout_u16(seed, offset,
  * bh, i, j) >= thr, and kept probabilities are multiplied by rs. */
 void fa_oracle_set_dropout(int enable, uint64_t seed, uint32_t offset, uint32_t thr, double rs) {
   t_dropout = enable;

@@ -474,8 +474,8 @@ def _z_scores(count, n, prob):
 
 
 def pin_dropout(orc):
-    """Dropout on P (O = (P o Z / (1 - p)) V, lse that of P), with Z replayed
-    from Philox4x32-10.
+    """Dropout on P (O = (P o Z / q) V with q the keep probability, lse that
+    of P), with Z replayed from Philox4x32-10.
 
     The generator against its published known-answer vectors; p = 0 against
     the plain definition (bit for bit); the keep decisions against their
@@ -502,25 +502,29 @@ def pin_dropout(orc):
         for a, b in zip(g0[:3], g1[:3]):
             assert np.array_equal(a, b), "p = 0 changes a gradient"
 
-    # keep decisions: rate, fair bits, independence
+    # keep decisions: the 16-bit values are the halves of the generator's
+    # words; rate, fair bits, independence
     p, seed, off = 0.2, 0x1234_5678_9ABC_DEF0, 7
     rows, cols = 48, 256
-    words = np.array([[orc.dropout_word(seed, off, 1, i, j) for j in range(cols)]
-                      for i in range(rows)], dtype=np.uint64)
-    n = words.size
+    u16 = np.array([[orc.dropout_u16(seed, off, 1, i, j) for j in range(cols)]
+                    for i in range(rows)], dtype=np.uint64)
+    words = orc.philox([0, 5, 1, off], [seed & 0xFFFFFFFF, seed >> 32])
+    assert [int(u16[5, 2 * e]) | (int(u16[5, 2 * e + 1]) << 16) for e in range(4)] == words
+    n = u16.size
     keep = orc.dropout_keep(p, seed, off, 1, rows, cols)
-    thr = int(np.floor(float(np.float32(p)) * 2**32))
-    assert np.array_equal(keep, words >= thr)
-    assert _z_scores(int(keep.sum()), n, 1.0 - p) < 5.0, "keep rate"
-    for b in range(32):
-        assert _z_scores(int(((words >> b) & 1).sum()), n, 0.5) < 5.0, f"bit {b} biased"
+    thr, rs = oracle_dropout_params(p)
+    assert thr == int(np.floor(float(np.float32(p)) * 65536)) and rs == 65536 / (65536 - thr)
+    assert np.array_equal(keep, u16 >= thr)
+    assert _z_scores(int(keep.sum()), n, 1.0 - thr / 65536) < 5.0, "keep rate"
+    for b in range(16):
+        assert _z_scores(int(((u16 >> b) & 1).sum()), n, 0.5) < 5.0, f"bit {b} biased"
     for other in ((seed, off, 0), (seed, off + 1, 1), (seed ^ 1, off, 1), (seed ^ 2**40, off, 1)):
-        keep2 = np.array([[orc.dropout_word(other[0], other[1], other[2], i, j) >= thr
+        keep2 = np.array([[orc.dropout_u16(other[0], other[1], other[2], i, j) >= thr
                            for j in range(cols)] for i in range(rows)])
         agree = int((keep == keep2).sum())
         assert _z_scores(agree, n, p * p + (1 - p) * (1 - p)) < 5.0, f"not independent {other}"
 
-    # V = identity: O_ij = P_ij Z_ij / (1 - p) exactly
+    # V = identity: O_ij = P_ij Z_ij / q exactly
     Nn = 24
     qq, kk = rng.standard_normal((2, Nn, Nn)), rng.standard_normal((2, Nn, Nn))
     eye = np.broadcast_to(np.eye(Nn), (2, Nn, Nn)).copy()

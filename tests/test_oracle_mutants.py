@@ -46,9 +46,13 @@ MUTANTS = [
      "const uint32_t y0 = (uint32_t)(p0 >> 32) ^ x1 ^ k0;"),
     ("dropout_counter_ignores_head", "(uint32_t)i, (uint32_t)bh, offset};",
      "(uint32_t)i, 0u, offset};"),
+    ("dropout_halves_swapped", "return (j % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);",
+     "return (j % 2 == 1) ? (word & 0xFFFFu) : (word >> 16);"),
+    ("dropout_word_index", "const uint32_t word = out[(j / 2) % 4];",
+     "const uint32_t word = out[j % 4];"),
     ("dropout_rescale_dropped", "? J->rs : 0.0;", "? 1.0 : 0.0;"),
-    ("dropout_ij_swapped", "fa_oracle_dropout_word(J->seed, J->offset, bh, i, j) >=",
-     "fa_oracle_dropout_word(J->seed, J->offset, bh, j, i) >="),
+    ("dropout_ij_swapped", "fa_oracle_dropout_u16(J->seed, J->offset, bh, i, j) >=",
+     "fa_oracle_dropout_u16(J->seed, J->offset, bh, j, i) >="),
     ("dropout_fwd_ignored", "if (J->dropout) /* dropout acts", "if (0) /* dropout acts"),
     ("dropout_dv_undropped", "dvj[c] += p * z * dOi[c];", "dvj[c] += p * dOi[c];"),
     ("dropout_col_dP_undropped", "dP *= z;", "(void)0;"),
