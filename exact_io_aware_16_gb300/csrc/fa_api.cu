@@ -287,17 +287,19 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
                        mask_head_stride, workspace, workspace_bytes, stream);
 }
 
-// Dropout parameters of probability p: keep iff the generator's word is
-// >= floor(p * 2^32), kept values times 1 / (1 - p).  p must lie in [0, 1);
-// p = 0 keeps everything and runs the kernels without dropout (returns false).
+// Dropout parameters of probability p: keep iff the element's 16 random bits
+// are >= thr16 = floor(p * 2^16), kept values times the inverse keep
+// probability 65536 / (65536 - thr16).  p must lie in [0, 1); thr16 = 0 keeps
+// everything and runs the kernels without dropout (*active = false).
 static int make_drop(float p, unsigned long long seed, unsigned int offset, fa::DropArgs* out,
                      bool* active) {
   if (!(p >= 0.0f && p < 1.0f)) return FA_ERR_SHAPE;  // also rejects NaN
-  *active = p > 0.0f;
+  const uint32_t thr16 = static_cast<uint32_t>(static_cast<double>(p) * 65536.0);  // floor
+  *active = thr16 > 0;
   out->set_seed(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
   out->offset = offset;
-  out->thr = static_cast<uint32_t>(static_cast<double>(p) * 4294967296.0);  // floor, < 2^32
-  out->rs = 1.0f / (1.0f - p);
+  out->thr_hi = thr16 << 16;
+  out->rs = static_cast<float>(65536.0 / (65536.0 - thr16));
   return FA_OK;
 }
 

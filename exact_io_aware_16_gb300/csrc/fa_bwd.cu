@@ -305,11 +305,12 @@ __device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bf
 // SPARSE: only the query tiles whose block-mask entry for this key tile is
 // set are visited (a compact list built by warp 0).
 //
-// DROPOUT (dropout on P with keep matrix Z and factor rs = 1 / (1 - p)):
+// DROPOUT (dropout on P with keep matrix Z and rs the inverse keep
+// probability):
 // dV = rs (P o Z)^T dO and dS = P o (rs Z o dP - D); P itself (undropped)
 // stays in registers for dS, P o Z goes to the dV product, rs is applied when
 // dV is stored.  The keep bits of a key row come transposed from the
-// generator's row-major counters (keep_nibble_t).
+// generator's row-major counters (keep_byte_t).
 template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq,
@@ -440,11 +441,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t kb[2] = {0u, 0u};
       if (DROPOUT) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          kb[u >> 3] |= keep_nibble_t(drop, static_cast<uint32_t>(krow),
-                                      static_cast<uint32_t>(q0) + col0 + 4u * u,
-                                      static_cast<uint32_t>(bh), lane)
-                        << (4 * (u & 7));
+        for (int u = 0; u < 8; ++u)
+          kb[u >> 2] |= keep_byte_t(drop, static_cast<uint32_t>(krow),
+                                    static_cast<uint32_t>(q0) + col0 + 8u * u,
+                                    static_cast<uint32_t>(bh), lane)
+                        << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x301)) {
@@ -693,11 +694,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // (bit c of kb[c / 32]), drawn before the scores are waited for
       uint32_t kb[2] = {0u, 0u};
       if (DROPOUT) {
-        const uint32_t jg0 = (static_cast<uint32_t>(kt_of(n)) * 128u + col0) >> 2;
+        const uint32_t jg0 = (static_cast<uint32_t>(kt_of(n)) * 128u + col0) >> 3;
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          kb[u >> 3] |= keep_nibble(drop, jg0 + u, static_cast<uint32_t>(row),
-                                    static_cast<uint32_t>(bh)) << (4 * (u & 7));
+        for (int u = 0; u < 8; ++u)
+          kb[u >> 2] |= keep_byte(drop, jg0 + u, static_cast<uint32_t>(row),
+                                  static_cast<uint32_t>(bh)) << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!bwd_warp_wait(&bars->s_full, n & 1, bars, 0x311)) {

@@ -28,8 +28,8 @@
 //     DROPOUT each thread draws the keep bits of its row for the next key
 //     tile from Philox4x32-10 (philox.cuh) while the tensor core computes the
 //     scores, zeroes dropped entries of P~ before the P V product (the row
-//     sum l keeps them: lse is that of P), and scales O by 1 / (1 - p) at
-//     the end.
+//     sum l keeps them: lse is that of P), and scales O by the inverse keep
+//     probability at the end.
 //
 // Ping-pong schedule of the MMA warp for key tile j:
 //     PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
@@ -310,11 +310,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // kb[c / 32] for key kv0 + c), drawn before the scores are waited for
       uint32_t kb[4] = {0u, 0u, 0u, 0u};
       if (DROPOUT) {
-        const uint32_t jg0 = static_cast<uint32_t>(kv_of(j) * kTileN) >> 2;
+        const uint32_t jg0 = static_cast<uint32_t>(kv_of(j) * kTileN) >> 3;
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          kb[u >> 3] |= keep_nibble(drop, jg0 + u, static_cast<uint32_t>(row),
-                                    static_cast<uint32_t>(bh)) << (4 * (u & 7));
+        for (int u = 0; u < 16; ++u)
+          kb[u >> 2] |= keep_byte(drop, jg0 + u, static_cast<uint32_t>(row),
+                                  static_cast<uint32_t>(bh)) << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!warp_wait(&bars->s_full[g], j & 1, bars, 0x301)) {

@@ -9,9 +9,11 @@
 // the key is bumped by two Weyl constants between rounds.
 //
 // Dropout on P (the talk's dropout applied to the attention probabilities
-// before the product with V): element (i, j) of head bh is kept iff word
-// j mod 4 of Philox(counter = (j / 4, i, bh, offset), key = seed) is at least
-// thr = floor(p * 2^32); kept probabilities are scaled by 1 / (1 - p).
+// before the product with V): one Philox call, counter = (j / 8, i, bh,
+// offset) and key = seed, decides eight consecutive keys of row i; key j
+// takes the low (even j) or high (odd j) 16 bits of word (j / 2) mod 4 and is
+// kept iff they are at least thr16 = floor(p * 2^16).  Kept probabilities are
+// scaled by the inverse keep probability 65536 / (65536 - thr16).
 #pragma once
 
 #include <cstdint>
@@ -27,8 +29,8 @@ struct DropArgs {
   uint32_t rk0[kPhiloxRounds] = {};  // round r key word 0: seed_lo + r * 0x9E3779B9
   uint32_t rk1[kPhiloxRounds] = {};  // round r key word 1: seed_hi + r * 0xBB67AE85
   uint32_t offset = 0;               // counter word 3
-  uint32_t thr = 0;                  // keep iff word >= thr
-  float rs = 1.0f;                   // 1 / (1 - p)
+  uint32_t thr_hi = 0;               // thr16 << 16: keep iff the 16 bits, moved up, are >= it
+  float rs = 1.0f;                   // 65536 / (65536 - thr16)
 
   __host__ __device__ void set_seed(uint32_t k0, uint32_t k1) {
     for (int r = 0; r < kPhiloxRounds; ++r) {
@@ -43,42 +45,52 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   constexpr uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
 #pragma unroll
   for (int r = 0; r < kPhiloxRounds; ++r) {
-    const uint32_t hi0 = __umulhi(kMul0, c0), lo0 = kMul0 * c0;
-    const uint32_t hi1 = __umulhi(kMul1, c2), lo1 = kMul1 * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ dr.rk0[r];
-    const uint32_t n2 = hi0 ^ c3 ^ dr.rk1[r];
+    // one 32 x 32 -> 64-bit multiply per product gives both halves
+    const uint64_t p0 = static_cast<uint64_t>(kMul0) * c0;
+    const uint64_t p1 = static_cast<uint64_t>(kMul1) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ dr.rk0[r];
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ dr.rk1[r];
     c0 = n0;
-    c1 = lo1;
+    c1 = static_cast<uint32_t>(p1);
     c2 = n2;
-    c3 = lo0;
+    c3 = static_cast<uint32_t>(p0);
   }
   return make_uint4(c0, c1, c2, c3);
 }
 
-// Keep bits of the four elements (i, 4 jg + e), e = 0..3, as bits 0..3.
-__device__ __forceinline__ uint32_t keep_nibble(const DropArgs& dr, uint32_t jg, uint32_t i,
-                                                uint32_t bh) {
-  const uint4 w = philox4x32_10(jg, i, bh, dr.offset, dr);
-  return static_cast<uint32_t>(w.x >= dr.thr) | (static_cast<uint32_t>(w.y >= dr.thr) << 1) |
-         (static_cast<uint32_t>(w.z >= dr.thr) << 2) | (static_cast<uint32_t>(w.w >= dr.thr) << 3);
+// The two decisions carried by one 32-bit word (low half: even key, high
+// half: odd key) as bits 0 and 1.  Comparing the halves moved to the top of
+// the word against thr16 << 16 decides them without masking.
+__device__ __forceinline__ uint32_t keep_pair(uint32_t w, uint32_t thr_hi) {
+  return static_cast<uint32_t>((w << 16) >= thr_hi) | (static_cast<uint32_t>(w >= thr_hi) << 1);
 }
 
-// Keep bits, transposed across a warp: lane L holds key row jrow (four
-// consecutive lanes hold four consecutive keys starting at a multiple of 4)
-// and wants the decisions for query rows i0 .. i0+3.  Each lane computes one
-// counter (its quad's key group, row i0 + L % 4) and four ballots hand every
-// lane its own key's column of the 4 x 4 block.  Returns the keep bits of
-// rows i0 + r as bits r = 0..3.  All 32 lanes must call it together.
-__device__ __forceinline__ uint32_t keep_nibble_t(const DropArgs& dr, uint32_t jrow, uint32_t i0,
-                                                  uint32_t bh, int lane) {
-  const uint32_t r = static_cast<uint32_t>(lane) & 3u;
-  const uint4 w = philox4x32_10(jrow >> 2, i0 + r, bh, dr.offset, dr);
-  const uint32_t b0 = __ballot_sync(0xffffffffu, w.x >= dr.thr);
-  const uint32_t b1 = __ballot_sync(0xffffffffu, w.y >= dr.thr);
-  const uint32_t b2 = __ballot_sync(0xffffffffu, w.z >= dr.thr);
-  const uint32_t b3 = __ballot_sync(0xffffffffu, w.w >= dr.thr);
-  const uint32_t mine = r == 0 ? b0 : (r == 1 ? b1 : (r == 2 ? b2 : b3));
-  return (mine >> (static_cast<uint32_t>(lane) & ~3u)) & 0xFu;
+// Keep bits of the eight elements (i, 8 jg + e), e = 0..7, as bits 0..7.
+__device__ __forceinline__ uint32_t keep_byte(const DropArgs& dr, uint32_t jg, uint32_t i,
+                                              uint32_t bh) {
+  const uint4 w = philox4x32_10(jg, i, bh, dr.offset, dr);
+  return keep_pair(w.x, dr.thr_hi) | (keep_pair(w.y, dr.thr_hi) << 2) |
+         (keep_pair(w.z, dr.thr_hi) << 4) | (keep_pair(w.w, dr.thr_hi) << 6);
+}
+
+// Keep bits, transposed across a warp: lane L holds key row jrow (eight
+// consecutive lanes hold eight consecutive keys starting at a multiple of 8)
+// and wants the decisions for query rows i0 .. i0+7.  Each lane computes one
+// counter (its octet's key group, row i0 + L % 8); eight ballots, one per key
+// of the group, hand every lane its own key's column of the 8 x 8 block.
+// Returns the keep bits of rows i0 + r as bits r = 0..7.  All 32 lanes must
+// call it together.
+__device__ __forceinline__ uint32_t keep_byte_t(const DropArgs& dr, uint32_t jrow, uint32_t i0,
+                                                uint32_t bh, int lane) {
+  const uint32_t r = static_cast<uint32_t>(lane) & 7u;
+  const uint32_t mine = keep_byte(dr, jrow >> 3, i0 + r, bh);  // row i0 + r, keys of the octet
+  uint32_t col = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t b = __ballot_sync(0xffffffffu, (mine >> e) & 1u);  // bit 8m + r: row r, key e
+    if (static_cast<uint32_t>(e) == r) col = b;
+  }
+  return (col >> (static_cast<uint32_t>(lane) & ~7u)) & 0xFFu;
 }
 
 }  // namespace fa

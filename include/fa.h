@@ -176,21 +176,24 @@ int fa_backward_blocksparse(const void* q, const void* k, const void* v, const v
 /*
  * Attention with dropout on the probabilities (the talk's dropout applied to
  * P before the product with V, fused with the softmax so P never reaches
- * memory):  O = (P o Z / (1 - p_drop)) V, with P = softmax(scale Q K^T) and
- * lse that of P (before dropout).
- *  - Z is replayed, never stored: element (i, j) of head bh = b*H + h is kept
- *    iff word j % 4 of Philox4x32-10 (Salmon et al., "Parallel random
- *    numbers: as easy as 1, 2, 3", SC 2011) at counter
- *    (j / 4, i, bh, offset) with key (seed & 0xffffffff, seed >> 32) is
- *    >= floor(p_drop * 2^32).  The backward must get the same p_drop, seed
- *    and offset as the forward; callers advance offset (or the seed) between
- *    independent draws.
- *  - 0 <= p_drop < 1, else FA_ERR_SHAPE.  p_drop = 0 runs the kernels of
- *    fa_forward / fa_backward (identical results).
+ * memory):  O = (P o Z / q) V, with P = softmax(scale Q K^T), q the keep
+ * probability and lse that of P (before dropout).
+ *  - Z is replayed, never stored.  One call of Philox4x32-10 (Salmon et al.,
+ *    "Parallel random numbers: as easy as 1, 2, 3", SC 2011) at counter
+ *    (j / 8, i, bh, offset), bh = b*H + h, with key (seed & 0xffffffff,
+ *    seed >> 32) gives 4 words that decide keys 8(j/8) .. 8(j/8)+7 of row
+ *    i: key j takes the low (even j) or high (odd j) 16 bits of word
+ *    (j / 2) % 4 and is kept iff they are >= thr16 = floor(p_drop * 2^16).
+ *    So q = 1 - thr16 / 65536 (p_drop taken to 16 bits), and kept values
+ *    are scaled by 1 / q exactly.  The backward must get the same p_drop,
+ *    seed and offset as the forward; callers advance offset (or the seed)
+ *    between independent draws.
+ *  - 0 <= p_drop < 1, else FA_ERR_SHAPE.  thr16 = 0 (p_drop < 2^-16) runs the
+ *    kernels of fa_forward / fa_backward (identical results).
  *  - block_mask: NULL for dense attention, else a block mask as for
  *    fa_forward_blocksparse (with its limits); dropout applies on top.
- *  - The backward gives the gradients of that O: dv = (P o Z)^T dO / (1 - p),
- *    dP = (dO V^T) o Z / (1 - p), dS = P o (dP - D), dq, dk as usual.
+ *  - The backward gives the gradients of that O: dv = (P o Z)^T dO / q,
+ *    dP = (dO V^T) o Z / q, dS = P o (dP - D), dq, dk as usual.
  * All other arguments, layouts and errors as for fa_forward / fa_backward.
  */
 int fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
