@@ -266,6 +266,9 @@ def run_ours(args, world, rank, local):
     D = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
+    if args.fp8:
+        del q, k, v, dO, o, lse, D, dq, dk, dv
+        return run_fp8(args, world, rank, local, fa, w, causal, stream, dev)
     if args.block_mask or args.dropout:
         return run_variant(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
     if args.decode:
@@ -516,6 +519,66 @@ def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     return 0
 
 
+def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
+    """e4m3 forward step: fa_forward_fp8 on the workload's q, k, v quantised
+    per tensor (fa_inputs.make_fp8_inputs).  Tensor-bound: FLOPs of the two
+    products (4 N^2 d per head, halved when causal) against the fp8 peak =
+    measured bf16 peak x 2 (the nominal fp8 : bf16 ratio)."""
+    from fa_inputs import make_fp8_inputs
+
+    if w.d != 128:
+        raise SystemExit("--fp8 needs a d = 128 workload")
+    q8, k8, _, vt8, ds = make_fp8_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    q, k, vt = (t.view(torch.uint8).to(dev) for t in (q8, k8, vt8))
+    del q8, k8, vt8
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+    def step():
+        fa.fa_forward_fp8(q, k, vt, *ds, causal=causal, scale=w.scale, o=o, lse=lse,
+                          stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    for s_ in range(args.steps):
+        evs[s_][0].record(stream)
+        step()
+        evs[s_][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, world)
+    f_fwd, _ = flops(w, causal)
+    peaks, peak_src = read_peaks()
+    peak = 2.0 * peaks["bf16_tflops"]
+    tf = f_fwd / (ms * 1e-3) / 1e12
+    if rank == 0:
+        cfg = workload_config(w, causal)
+        cfg.update({"inputs": "e4m3 q, k, V^T with per-tensor descales (amax / 448)",
+                    "l2": "inputs (q, k, v e4m3 = 201 MB per step) larger than L2"})
+        line = {
+            "metric": "attention forward TFLOP/s at 1 GB300, e4m3 inputs",
+            "value": world * tf, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "tensor", "kernel": "fwd_fp8", "achieved": tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "peak_kind": f"fp8 = 2 x burst bf16 ({peak_src})"},
+            "gpu_launches": args.steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
     """Decode step: the last --decode query rows against the whole key/value
     cache of the workload (causal: query i at position N - Nq + i).  HBM-bound:
@@ -587,6 +650,8 @@ def main():
                     help="time the block-sparse path with mask band:W[:G] (tiles of 128)")
     ap.add_argument("--dropout", type=float, default=None,
                     help="time the dropout path with this probability (0 < p < 1)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the e4m3 forward (fa_forward_fp8) on the workload")
     ap.add_argument("--decode", type=int, default=None,
                     help="time the decode step with this many query rows (<= 16)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     fa_forward,
     fa_forward_blocksparse,
     fa_forward_dropout,
+    fa_forward_fp8,
     fa_forward_tile_count,
     fa_get_device_error,
     fa_status_string,
@@ -30,7 +31,7 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "FaError", "fa_forward", "fa_backward", "fa_decode", "fa_decode_workspace_size", "fa_forward_blocksparse", "fa_backward_blocksparse",
-    "fa_forward_dropout", "fa_backward_dropout", "fa_backward_preprocess", "fa_backward_dkdv",
+    "fa_forward_dropout", "fa_backward_dropout", "fa_forward_fp8", "fa_backward_preprocess", "fa_backward_dkdv",
     "fa_backward_dq", "fa_backward_noalloc",
     "fa_backward_workspace_size", "fa_forward_tile_count", "fa_get_device_error",
     "fa_status_string", "library", "library_path",

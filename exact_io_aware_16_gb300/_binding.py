@@ -67,6 +67,8 @@ def library():
         lib.fa_backward_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i,
                                             f, u64, u32, vp, ll, vp, sz, vp]
         lib.fa_backward_dropout.restype = i
+        lib.fa_forward_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_forward_fp8.restype = i
         lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -249,6 +251,36 @@ def fa_backward_dropout(q, k, v, o, dO, lse, p_drop: float, seed: int, offset: i
     if st != FA_OK:
         raise FaError(st, "fa_backward_dropout")
     return dq, dk, dv
+
+
+def fa_forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: float,
+                   causal: bool = False, scale: float | None = None, o=None, lse=None,
+                   stream=None):
+    """O and lse of the attention of the dequantised e4m3 inputs.
+
+    q8, k8: torch.float8_e4m3fn (or uint8 holding e4m3) [B,H,N,d]; vt8: V
+    transposed per head, [B,H,d,N]; the descales map stored values to real
+    ones.  d = 128, N a multiple of 16.
+    """
+    B, H, N, d = q8.shape
+    for t, nm, shp in ((q8, "q8", (B, H, N, d)), (k8, "k8", (B, H, N, d)),
+                       (vt8, "vt8", (B, H, d, N))):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{nm} must be a contiguous one-byte (e4m3) CUDA tensor")
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{nm} has shape {tuple(t.shape)}, expected {shp}")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    st = library().fa_forward_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), float(q_descale),
+                                  float(k_descale), float(v_descale), _ptr(o), _ptr(lse), B, H,
+                                  N, d, float(scale), int(bool(causal)),
+                                  ctypes.c_void_p(_stream_handle(stream, q8.device)))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward_fp8")
+    return o, lse
 
 
 def fa_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:

@@ -77,6 +77,24 @@ int encode_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int ro
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// A [BH][rows][cols] uint8 (e4m3) tensor as a 3-D tensor (cols, rows, BH);
+// box 128 x 128 x 1 (128-byte rows, 128-byte swizzle).  cols must be a
+// multiple of 16 (row stride in bytes).
+int encode_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
 }  // namespace
@@ -330,6 +348,45 @@ int fa_backward_dropout(const void* q, const void* k, const void* v, const void*
   return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, block_mask,
                        block_mask ? mask_head_stride : 0, workspace, workspace_bytes, stream,
                        active ? &dr : nullptr);
+}
+
+int fa_forward_fp8(const void* q8, const void* k8, const void* vt8, float q_descale,
+                   float k_descale, float v_descale, void* o, float* lse, int B, int H, int N,
+                   int d, float scale, int causal, void* stream) {
+  if (!q8 || !k8 || !vt8 || !o || !lse) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_HEADDIM;
+  if (N % 16 != 0) return FA_ERR_SHAPE;  // rows of V^T must be 16-byte aligned
+  if ((st = check_scale(scale)) != FA_OK || (st = check_scale(q_descale)) != FA_OK ||
+      (st = check_scale(k_descale)) != FA_OK || (st = check_scale(v_descale)) != FA_OK)
+    return st;
+  const double s2 = static_cast<double>(scale) * q_descale * k_descale;
+  if (!std::isfinite(s2) || !(s2 > 0.0) || !std::isfinite(static_cast<float>(s2)))
+    return FA_ERR_SHAPE;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if ((st = check_arch()) != FA_OK) return st;
+  const int BH = B * H;
+  fa::TensorMaps maps;
+  if (encode_u8(&maps.q, q8, BH, N, d) != FA_OK || encode_u8(&maps.k, k8, BH, N, d) != FA_OK ||
+      encode_u8(&maps.v, vt8, BH, d, N) != FA_OK)
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.tq = &maps.q;
+  a.tk = &maps.k;
+  a.tv = &maps.v;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = static_cast<float>(s2 * 1.4426950408889634);
+  a.causal = causal ? 1 : 0;
+  a.fp8 = true;
+  a.o_scale = v_descale;
+  cudaError_t e = fa::launch_forward(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 static int check_decode_shape(int B, int H, int Nq, int Nk, int d) {

@@ -61,10 +61,12 @@ constexpr int kStages = 2;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLazyRescaleLog2 = 8.0f;
 
-template <int D>
+// EB: bytes per element of Q, K, V (2: bf16, 1: e4m3).  A tile is 128 rows;
+// every 128-byte run of a row is one swizzled TMA box column ("chunk").
+template <int D, int EB = 2>
 struct FwdLayout {
-  static constexpr int kChunks = D / 64;
-  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr int kChunks = D * EB / 128;
+  static constexpr uint32_t kTileBytes = 128u * D * EB;
   static constexpr uint32_t kQ = 0;  // two Q tiles
   static constexpr uint32_t kK = kQ + 2 * kTileBytes;
   static constexpr uint32_t kV = kK + kStages * kTileBytes;
@@ -106,13 +108,22 @@ __device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity, FwdBars
 // (entry = key tile | keep-by-tile-0 << 14 | keep-by-tile-1 << 15); for each
 // list entry both query tiles compute their scores, and a query tile that
 // does not keep the key tile masks all of it to -inf.
-template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
+//
+// FP8: Q, K and V are e4m3 (V transposed per head, [d][N], so that both
+// products read K-major operands); S = Q K^T and O += P V are
+// tcgen05.mma.kind::f8f6f4 (K = 32 per instruction), P~ is rounded to e4m3
+// into tensor memory as the A operand of P V, and o_scale (the V descale)
+// multiplies O in the epilogue.  The Q and K descales are folded into
+// scale_log2 by the caller.
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int BH, int N, float scale_log2,
-                  const uint8_t* __restrict__ bmask, long long mstride, DropArgs drop) {
-  using L = FwdLayout<D>;
+                  const uint8_t* __restrict__ bmask, long long mstride, DropArgs drop,
+                  float o_scale) {
+  static_assert(!FP8 || (D == 128 && !SPARSE && !DROPOUT), "e4m3 path: d = 128, dense");
+  using L = FwdLayout<D, FP8 ? 1 : 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -213,10 +224,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       kt * kTileN, bh);
         if (!mbar_wait(&bars->v_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x102)) break;
         mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+        if (FP8) {  // V^T tile: d rows of 128 keys
+          tma_load_3d(smem + L::kV + s * L::kTileBytes, &tv, &bars->v_full[s], kt * kTileN, 0,
+                      bh);
+        } else {
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s], c * 64,
-                      kt * kTileN, bh);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s],
+                        c * 64, kt * kTileN, bh);
+        }
       }
     }
     __syncwarp();
@@ -225,24 +241,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idesc_f8 = idesc_e4m3_f32(128, 128);
       auto issue_s = [&](int g, int j) {
         const uint32_t kbase = sK + (j % kStages) * L::kTileBytes;
         const uint32_t qbase = sQ + g * L::kTileBytes;
+        if (FP8) {  // K = 32 e4m3 = 32 bytes per instruction, one 128-byte chunk
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + L::s_col(g), sdesc_sw128(qbase + off, 16, 1024),
-                  sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            umma_ss_f8(tmem + L::s_col(g), sdesc_sw128(qbase + kk * 32, 16, 1024),
+                       sdesc_sw128(kbase + kk * 32, 16, 1024), idesc_f8, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_ss(tmem + L::s_col(g), sdesc_sw128(qbase + off, 16, 1024),
+                    sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
         umma_commit(&bars->s_full[g]);
       };
       auto issue_pv = [&](int g, int j) {
         const uint32_t vbase = sV + (j % kStages) * L::kTileBytes;
+        if (FP8) {  // A = P~ e4m3, 8 tensor-memory columns per 32 keys; B = V^T K-major
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          umma_ts(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
-                  sdesc_sw128(vbase + kk * 2048, 16384, 1024), idesc_pv,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTileN / 32; ++kk)
+            umma_ts_f8(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
+                       sdesc_sw128(vbase + kk * 32, 16, 1024), idesc_f8,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            umma_ts(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
+                    sdesc_sw128(vbase + kk * 2048, 16384, 1024), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&bars->pv_done[g]);
       };
       bool ok = n1 > 0 && mma_wait(&bars->q_full, 0, bars, 0x201) &&
@@ -363,22 +395,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
-      // P~ packed in place: pair c overwrites sr[c], already consumed
+      if (FP8) {
+        // P~ as e4m3, four per word: quad c overwrites sr[c], already consumed
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
-        sp[c & 7] += p0 + p1;
-        if (DROPOUT) {
-          const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
-          sr[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
-        } else {
-          sr[c] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 32; ++c) {
+          float pq[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pq[e] = ex2_approx(fmaf(__uint_as_float(sr[4 * c + e]), scale_log2, -m_use));
+          sp[(2 * c) & 7] += pq[0] + pq[1];
+          sp[(2 * c + 1) & 7] += pq[2] + pq[3];
+          sr[c] = pack_e4m3x4(pq[0], pq[1], pq[2], pq[3]);
+        }
+      } else {
+        // P~ packed in place: pair c overwrites sr[c], already consumed
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
+          sp[c & 7] += p0 + p1;
+          if (DROPOUT) {
+            const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
+            sr[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+          } else {
+            sr[c] = pack_bf16x2(p0, p1);
+          }
         }
       }
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      if (!FP8) tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       if (move && j > 0) {
         // PV_g(j-1) completed before S_g(j) was reported, and PV_g(j) is not
         // issued before p_ready: O is stable here
@@ -411,7 +457,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after_sync();
       // a row with no visible key (block-sparse) has l = 0: O = 0, lse = -inf;
       // with dropout the kept terms carry the factor 1 / (1 - p)
-      const float inv_l = l_run > 0.0f ? (DROPOUT ? drop.rs : 1.0f) / l_run : 0.0f;
+      const float inv_l =
+          l_run > 0.0f ? (DROPOUT ? drop.rs : 1.0f) * (FP8 ? o_scale : 1.0f) / l_run : 0.0f;
       __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -455,10 +502,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8 = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE, DROPOUT>;
-  constexpr uint32_t smem = FwdLayout<D>::kSmem;
+  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE, DROPOUT, FP8>;
+  constexpr uint32_t smem = FwdLayout<D, FP8 ? 1 : 2>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long nq = (a.N + kTileM - 1) / kTileM;
@@ -466,7 +513,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
-      a.bmask, a.mstride, a.drop);
+      a.bmask, a.mstride, a.drop, a.o_scale);
   return cudaGetLastError();
 }
 
@@ -482,6 +529,10 @@ cudaError_t launch_forward_s(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
+  if (a.fp8) {  // d = 128, dense, no dropout (checked by the caller)
+    return a.causal ? launch_fwd_t<128, true, false, false, true>(a, s)
+                    : launch_fwd_t<128, false, false, false, true>(a, s);
+  }
   if (a.dropout)
     return a.bmask ? launch_forward_s<true, true>(a, s) : launch_forward_s<false, true>(a, s);
   return a.bmask ? launch_forward_s<true, false>(a, s) : launch_forward_s<false, false>(a, s);

@@ -37,6 +37,8 @@ struct FwdArgs {
   long long mstride = 0;           // elements between (b,h) masks (0: one shared mask)
   bool dropout = false;            // dropout on P with the parameters in drop
   DropArgs drop;
+  bool fp8 = false;                // e4m3 Q, K and V^T (tv maps V^T [BH][d][N])
+  float o_scale = 1.0f;            // e4m3: V descale, applied to O
 };
 
 struct BwdArgs {

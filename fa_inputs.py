@@ -8,6 +8,11 @@ Recipe: one CPU ``torch.Generator`` seeded with ``seed`` draws, in this order,
 full tensors q, k, v and dO of shape [B, H, N, d], each fp32 N(0, 1); q and k
 are multiplied by ``qk_mult`` (x2 is exact in bf16) and every tensor is cast
 to bf16 with round-to-nearest-even.  ``scale`` defaults to 1/sqrt(d).
+
+e4m3 inputs (``make_fp8_inputs``): the same fp32 draws of q, k, v, each
+divided by its per-tensor descale amax / 448 (448 = largest finite e4m3)
+and rounded to e4m3 (round to nearest even); V is also given transposed per
+head, [B, H, d, N].
 """
 from __future__ import annotations
 
@@ -72,6 +77,39 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int = 0, qk_mult: float = 
     v = v.to(torch.bfloat16)
     dO = dO.to(torch.bfloat16) if dO is not None else None
     return q, k, v, dO
+
+
+E4M3_MAX = 448.0
+
+
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int = 0, qk_mult: float = 1.0):
+    """e4m3 CPU tensors and their per-tensor descales.
+
+    Returns (q8, k8, v8, vt8, descales): q8, k8, v8 torch.float8_e4m3fn of
+    shape [B, H, N, d], vt8 = v8 transposed to [B, H, d, N] (contiguous),
+    descales = (q_descale, k_descale, v_descale) as Python floats that are
+    exact fp32 values; the real inputs are q8 * q_descale etc.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (B, H, N, d)
+    xs = [torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(3)]
+    if qk_mult != 1.0:
+        xs[0].mul_(qk_mult)
+        xs[1].mul_(qk_mult)
+    out, desc = [], []
+    for x in xs:
+        ds = float(torch.tensor(float(x.abs().max()) / E4M3_MAX, dtype=torch.float32))
+        out.append((x / ds).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn))
+        desc.append(ds)
+    q8, k8, v8 = out
+    vt8 = v8.transpose(-1, -2).contiguous()
+    return q8, k8, v8, vt8, tuple(desc)
+
+
+def dequantize(x8, descale: float):
+    """The real values of an e4m3 tensor, exactly, as float64."""
+    return x8.to(torch.float64) * float(descale)
 
 
 def workload_inputs(w: Workload, with_dO: bool = True):

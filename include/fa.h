@@ -208,6 +208,31 @@ int fa_backward_dropout(const void* q, const void* k, const void* v, const void*
                         void* stream);
 
 /*
+ * FP8 forward (e4m3 inputs, FlashAttention-3's FP8 mode named on the pages):
+ * O = softmax(scale * Qd Kd^T) Vd with Qd = q_descale * q8 (likewise K, V),
+ * i.e. exact attention of the dequantised inputs, computed with e4m3 tensor
+ * core products: S = q8 k8^T in fp32, P rounded to e4m3 for the P V
+ * product, fp32 accumulation, O and lse as for fa_forward.
+ *  - q8, k8: DEVICE e4m3 (one byte each, IEEE-style 1-4-3 with bias 7, no
+ *    infinities) [B][H][N][d].  vt8: V TRANSPOSED per head, e4m3
+ *    [B][H][d][N] (element (b,h,c,j) at ((b*H + h)*d + c)*N + j), so that
+ *    both products read their operands K-major.
+ *  - q_descale, k_descale, v_descale: per-tensor factors (> 0, finite) that
+ *    map the stored e4m3 values back to the real inputs.
+ *  - o: bf16 [B][H][N][d]; lse: fp32 [B][H][N], logsumexp of the scaled
+ *    scores of the dequantised inputs.
+ *  - d must be 128 (FA_ERR_HEADDIM otherwise); N must be a multiple of 16
+ *    (rows of vt8 are 16-byte aligned), else FA_ERR_SHAPE.
+ *  - Accuracy: besides bf16 output rounding, the one approximation is the
+ *    e4m3 rounding of each probability (relative 2^-4, absolute 2^-10
+ *    below the normal range) before the P V product.
+ * Other conventions as for fa_forward.
+ */
+int fa_forward_fp8(const void* q8, const void* k8, const void* vt8, float q_descale,
+                   float k_descale, float v_descale, void* o, float* lse, int B, int H, int N,
+                   int d, float scale, int causal, void* stream);
+
+/*
  * Decode step: Nq new query rows against an Nk-row key/value cache (the KV
  * cache the transcript of "What is Flash Attention?" names as the next stop,
  * 11:33).  q [B][H][Nq][d], k and v [B][H][Nk][d] bf16; o [B][H][Nq][d] bf16,

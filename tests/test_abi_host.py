@@ -120,6 +120,21 @@ def test_dropout_validation(lib):
     assert bw(w=None) == -6
 
 
+def test_fp8_validation(lib):
+    f = lib.fa_forward_fp8
+
+    def fw(N=256, d=128, qd=1.0, q=FAKE, scale=0.125):
+        return f(q, FAKE, FAKE, qd, 1.0, 1.0, FAKE, FAKE, 1, 2, N, d, scale, 0, None)
+
+    assert fw(q=None) == -1
+    assert fw(d=64) == -3
+    assert fw(N=100) == -2  # not a multiple of 16
+    assert fw(qd=0.0) == -2
+    assert fw(qd=float("nan")) == -2
+    assert fw(scale=-1.0) == -2
+    assert fw(qd=1e30, scale=1e30) == -2  # folded score scale overflows
+
+
 def test_decode_validation(lib):
     ws = lib.fa_decode_workspace_size(2, 4, 8, 1000, 128)
     assert ws > 0 and ws % 256 == 0
