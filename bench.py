@@ -347,7 +347,8 @@ def run_ours(args, world, rank, local):
     if dom == "bwd_pre":
         ach = kbytes[dom] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None}
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": captured_traffic(dom, w.name) if causal == w.causal[0] else None}
     else:
         ach = kflops[dom] / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
@@ -511,7 +512,10 @@ def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
             "data": "synthetic", "config": cfg, "fwd_tflops": fwd_tf,
             "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "kernel": "fwd", "achieved": fwd_tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": fwd_tf / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": fwd_tf / peak,
+                         "traffic": (captured_traffic("fwd_dropout", w.name)
+                                     if (p_drop == 0.1 and mask_cpu is None
+                                         and causal == w.causal[0]) else None),
                          "peak_kind": f"burst bf16 ({peak_src})"},
             "gpu_launches": 4 * args.steps, "clocks": clk,
         }
@@ -571,7 +575,9 @@ def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
             "data": "synthetic", "config": cfg,
             "roofline": {"bound": "tensor", "kernel": "fwd_fp8", "achieved": tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": tf / peak,
+                         "traffic": (captured_traffic("fwd_fp8", w.name)
+                                     if causal == w.causal[0] else None),
                          "peak_kind": f"fp8 = 2 x burst bf16 ({peak_src})"},
             "gpu_launches": args.steps, "clocks": clk,
         }
