@@ -635,7 +635,7 @@ def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": cfg,
-            "roofline": {"bound": "hbm", "kernel": "decode_split+combine", "achieved": gbs,
+            "roofline": {"bound": "hbm", "kernel": "decode_split_tc+decode_combine", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                          "traffic": None, "peak_kind": peak_src},
             "gpu_launches": 2 * args.steps, "clocks": clk,

@@ -95,6 +95,19 @@ int encode_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// SM count of the current device (cached per device ordinal).
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  static int cache[64];
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
 }  // namespace
@@ -429,7 +442,7 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.Nq = Nq;
   a.Nk = Nk;
   a.d = d;
-  a.S = fa::decode_splits(a.BH, Nk);
+  a.S = fa::decode_splits_run(a.BH, Nk, num_sms());
   a.chunk = ((Nk + a.S - 1) / a.S + 63) / 64 * 64;
   a.S = (Nk + a.chunk - 1) / a.chunk;  // no empty ranges
   a.scale = scale;
@@ -439,16 +452,23 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   // partial lse after the partial outputs, 256-byte aligned
   a.part_lse = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(a.part_o + n_o) + 255) & ~static_cast<uintptr_t>(255));
-  cudaError_t e = fa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  fa::TensorMaps maps;
+  if (encode_bhnd(&maps.q, q, a.BH, Nq, d, 128) != FA_OK ||
+      encode_bhnd(&maps.k64, k, a.BH, Nk, d, 64) != FA_OK ||
+      encode_bhnd(&maps.v64, v, a.BH, Nk, d, 64) != FA_OK)
+    return FA_ERR_CUDA;
+  cudaError_t e =
+      fa::launch_decode(a, &maps.q, &maps.k64, &maps.v64, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_get_device_error(void* stream, uint32_t* detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t w_fwd = 0, w_bwd = 0;
+  uint32_t w_fwd = 0, w_bwd = 0, w_dtc = 0;
   if (fa::fwd_read_clear_error(&w_fwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::bwd_read_clear_error(&w_bwd, s) != cudaSuccess) return FA_ERR_CUDA;
-  const uint32_t w = w_fwd ? w_fwd : w_bwd;
+  if (fa::dtc_read_clear_error(&w_dtc, s) != cudaSuccess) return FA_ERR_CUDA;
+  const uint32_t w = w_fwd ? w_fwd : (w_bwd ? w_bwd : w_dtc);
   if (detail) *detail = w;
   return w ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }

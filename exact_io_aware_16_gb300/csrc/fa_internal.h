@@ -74,9 +74,9 @@ struct DecodeArgs {
   int causal;
 };
 
-// Number of key ranges a decode step is split into (shape-only, so the
-// workspace size needs no device): enough CTAs for four waves of 152 SMs,
-// ranges of at least 256 keys.
+// Upper bound on the number of key ranges of a decode step (shape-only, so
+// the workspace size needs no device): four waves of 152 SMs, ranges of at
+// least 256 keys.
 inline int decode_splits(long long BH, int Nk) {
   const long long by_len = (Nk + 255) / 256;
   long long by_sms = (608 + BH - 1) / BH;
@@ -85,8 +85,23 @@ inline int decode_splits(long long BH, int Nk) {
   return static_cast<int>(s < 1 ? 1 : s);
 }
 
+// Key ranges a decode step actually uses: one wave of two CTAs per SM,
+// ranges of at least 256 keys, never more than decode_splits().
+inline int decode_splits_run(long long BH, int Nk, int num_sms) {
+  const long long by_len = (Nk + 255) / 256;
+  long long by_sms = (2ll * num_sms) / BH;
+  if (by_sms < 1) by_sms = 1;
+  long long s = by_len < by_sms ? by_len : by_sms;
+  const long long cap = decode_splits(BH, Nk);
+  if (s > cap) s = cap;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// Decode (split on the tensor core, then combine): tq maps q as (d, Nq, BH)
+// with 128-row boxes, tk / tv map k / v as (d, Nk, BH) with 64-row boxes.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
+                          const CUtensorMap* tv, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                   cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
@@ -95,6 +110,7 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
 // Device error words of each kernel translation unit: read-and-clear.
 cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s);
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s);
+cudaError_t dtc_read_clear_error(uint32_t* out, cudaStream_t s);
 
 // Tile counts (host-side mirror of the kernels' loop bounds).
 inline int num_tiles(int N, int tile) { return (N + tile - 1) / tile; }

@@ -32,6 +32,11 @@ CASES = [
     (1, 1, 16, 16, 128, True),
     (3, 1, 3, 1, 64, False),
     (1, 4, 8, 20000, 128, True),
+    (1, 3, 4, 1000, 128, True),     # the first query count on the tensor core
+    (2, 2, 5, 1000, 64, False),
+    (1, 2, 16, 129, 128, True),     # a 64-key tile with one key in it
+    (4, 80, 6, 3000, 128, True),    # more heads than CTA slots: one range per head
+    (1, 1, 12, 65536, 64, True),
 ]
 
 
