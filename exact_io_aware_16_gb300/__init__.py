@@ -8,6 +8,7 @@ sm_103, the calls raise.
 """
 from ._binding import (  # noqa: F401
     FaError,
+    HostPlan,
     fa_backward,
     fa_backward_blocksparse,
     fa_backward_dkdv,
@@ -30,7 +31,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = [
-    "FaError", "fa_forward", "fa_backward", "fa_decode", "fa_decode_workspace_size", "fa_forward_blocksparse", "fa_backward_blocksparse",
+    "FaError", "HostPlan", "fa_forward", "fa_backward", "fa_decode", "fa_decode_workspace_size", "fa_forward_blocksparse", "fa_backward_blocksparse",
     "fa_forward_dropout", "fa_backward_dropout", "fa_forward_fp8", "fa_backward_preprocess", "fa_backward_dkdv",
     "fa_backward_dq", "fa_backward_noalloc",
     "fa_backward_workspace_size", "fa_forward_tile_count", "fa_get_device_error",

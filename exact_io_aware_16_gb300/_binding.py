@@ -69,6 +69,14 @@ def library():
         lib.fa_backward_dropout.restype = i
         lib.fa_forward_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_forward_fp8.restype = i
+        lib.fa_host_plan_create.argtypes = [i, i, i, i, f, i, ctypes.POINTER(vp)]
+        lib.fa_host_plan_create.restype = i
+        lib.fa_host_step.argtypes = [vp] * 10
+        lib.fa_host_step.restype = i
+        lib.fa_host_wait.argtypes = [vp]
+        lib.fa_host_wait.restype = i
+        lib.fa_host_plan_destroy.argtypes = [vp]
+        lib.fa_host_plan_destroy.restype = i
         lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -281,6 +289,69 @@ def fa_forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: f
     if st != FA_OK:
         raise FaError(st, "fa_forward_fp8")
     return o, lse
+
+
+class HostPlan:
+    """Training steps on HOST tensors through the library's host runtime
+    (fa_host_plan_create / fa_host_step / fa_host_wait).
+
+    step() enqueues one fa_forward + fa_backward whose inputs q, k, v, dO and
+    outputs o, lse, dq, dk, dv are CPU tensors (bf16 [B,H,N,d], lse fp32
+    [B,H,N]; pin them for the copies to overlap the kernels) and returns at
+    once; the tensors must stay untouched until wait().
+    """
+
+    def __init__(self, B: int, H: int, N: int, d: int, causal: bool = False,
+                 scale: float | None = None, device=None):
+        self.shape = (B, H, N, d)
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        lib = library()
+        h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            st = lib.fa_host_plan_create(B, H, N, d, float(scale), int(bool(causal)),
+                                         ctypes.byref(h))
+        if st != FA_OK:
+            raise FaError(st, "fa_host_plan_create")
+        self._h = h
+        self._keep = []
+
+    def step(self, q, k, v, dO, o, lse, dq, dk, dv):
+        B, H, N, d = self.shape
+        for t, nm in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO"), (o, "o"), (dq, "dq"),
+                      (dk, "dk"), (dv, "dv")):
+            if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous() \
+                    or tuple(t.shape) != (B, H, N, d):
+                raise TypeError(f"{nm} must be a contiguous bf16 CPU tensor of shape "
+                                f"{(B, H, N, d)}")
+        if lse.device.type != "cpu" or lse.dtype != torch.float32 or not lse.is_contiguous() \
+                or tuple(lse.shape) != (B, H, N):
+            raise TypeError(f"lse must be a contiguous fp32 CPU tensor of shape {(B, H, N)}")
+        ts = (q, k, v, dO, o, lse, dq, dk, dv)
+        st = library().fa_host_step(self._h, *(ctypes.c_void_p(t.data_ptr()) for t in ts))
+        if st != FA_OK:
+            raise FaError(st, "fa_host_step")
+        self._keep.append(ts)  # the buffers stay referenced until wait()
+
+    def wait(self):
+        st = library().fa_host_wait(self._h)
+        self._keep.clear()
+        if st != FA_OK:
+            raise FaError(st, "fa_host_wait")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            st = library().fa_host_plan_destroy(self._h)
+            self._h = None
+            self._keep.clear()
+            if st != FA_OK:
+                raise FaError(st, "fa_host_plan_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fa_decode_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int) -> int:

@@ -250,6 +250,37 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
               size_t workspace_bytes, void* stream);
 
 /*
+ * Host-buffer runtime: training steps (fa_forward + fa_backward) whose
+ * inputs and outputs live in HOST memory.  The paper has no counterpart
+ * (its kernels start from tensors in HBM); this is the call a host program
+ * makes when its data arrive from and return to the CPU side.
+ *  - fa_host_plan_create: fixes B, H, N, d, scale, causal; allocates, on the
+ *    current device, the device buffers of two step slots (q, k, v, dO, o,
+ *    lse, dq, dk, dv and the backward workspace each), and three streams.
+ *    The only allocating call of this runtime; FA_ERR_CUDA if it fails.
+ *  - fa_host_step: enqueues one step and returns without waiting: copy q, k,
+ *    v, dO ([B][H][N][d] bf16, host) in, run the step, copy o (bf16), lse
+ *    (fp32 [B][H][N]), dq, dk, dv out to the host buffers given.  Steps
+ *    alternate between the two slots; the copies of the next and previous
+ *    steps overlap the kernels of this one.  Host buffers must stay valid
+ *    and untouched until fa_host_wait returns; page-locked (pinned) host
+ *    memory is needed for the copies to overlap (other memory works, with
+ *    copies that block the calling thread).
+ *  - fa_host_wait: blocks until every enqueued step has finished and its
+ *    outputs are in host memory; returns the first device error, as
+ *    fa_get_device_error does.
+ *  - fa_host_plan_destroy: waits, then frees the plan (NULL is a no-op).
+ * Argument errors as for fa_forward; NULL pointers give FA_ERR_NULL.
+ */
+typedef struct fa_host_plan fa_host_plan;
+int fa_host_plan_create(int B, int H, int N, int d, float scale, int causal,
+                        fa_host_plan** plan);
+int fa_host_step(fa_host_plan* plan, const void* q, const void* k, const void* v,
+                 const void* dO, void* o, float* lse, void* dq, void* dk, void* dv);
+int fa_host_wait(fa_host_plan* plan);
+int fa_host_plan_destroy(fa_host_plan* plan);
+
+/*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library timed out in a pipeline wait since the last call (and clears
  * the record), FA_ERR_CUDA if the synchronisation failed, else FA_OK.

@@ -135,6 +135,19 @@ def test_fp8_validation(lib):
     assert fw(qd=1e30, scale=1e30) == -2  # folded score scale overflows
 
 
+def test_host_plan_validation(lib):
+    h = ctypes.c_void_p()
+    f = lib.fa_host_plan_create
+    assert f(1, 1, 128, 64, 0.125, 0, None) == -1
+    assert f(0, 1, 128, 64, 0.125, 0, ctypes.byref(h)) == -2
+    assert f(1, 1, 128, 96, 0.125, 0, ctypes.byref(h)) == -3
+    assert f(1, 1, 128, 64, float("nan"), 0, ctypes.byref(h)) == -2
+    assert h.value is None  # nothing was created
+    assert lib.fa_host_step(None, *([FAKE] * 9)) == -1
+    assert lib.fa_host_wait(None) == -1
+    assert lib.fa_host_plan_destroy(None) == 0
+
+
 def test_decode_validation(lib):
     ws = lib.fa_decode_workspace_size(2, 4, 8, 1000, 128)
     assert ws > 0 and ws % 256 == 0
