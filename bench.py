@@ -636,7 +636,8 @@ def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
             "dtype": "bf16", "data": "synthetic", "config": cfg,
             "roofline": {"bound": "hbm", "kernel": "decode_split_tc+decode_combine", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": None, "peak_kind": peak_src},
+                         "traffic": captured_traffic("decode", cfg["workload"]),
+                         "peak_kind": peak_src},
             "gpu_launches": 2 * args.steps, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
