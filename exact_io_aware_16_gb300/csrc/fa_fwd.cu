@@ -373,17 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      // row max as a tree of 8 independent partial maxima (short dependency chains)
-      float mp[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mp[e] = __uint_as_float(sr[e]);
-#pragma unroll
-      for (int c = 8; c < 128; c += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], __uint_as_float(sr[c + e]));
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      const float m_blk = mx * scale_log2;
+      const float m_blk = row_max128(sr) * scale_log2;
       // move the running max only when some row of the warp needs it
       const bool move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
       float alpha = 1.0f;
@@ -394,26 +384,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+      // exponent arguments and row sums two lanes at a time (packed fp32 FMA / add)
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 sp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};  // partial row sums
       if (FP8) {
         // P~ as e4m3, four per word: quad c overwrites sr[c], already consumed
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          float pq[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pq[e] = ex2_approx(fmaf(__uint_as_float(sr[4 * c + e]), scale_log2, -m_use));
-          sp[(2 * c) & 7] += pq[0] + pq[1];
-          sp[(2 * c + 1) & 7] += pq[2] + pq[3];
-          sr[c] = pack_e4m3x4(pq[0], pq[1], pq[2], pq[3]);
+          const float2 x01 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), sc2, nm2);
+          const float2 x23 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])), sc2,
+              nm2);
+          const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+          const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+          sp[(2 * c) & 3] = __fadd2_rn(sp[(2 * c) & 3], p01);
+          sp[(2 * c + 1) & 3] = __fadd2_rn(sp[(2 * c + 1) & 3], p23);
+          sr[c] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
         }
       } else {
-        // P~ packed in place: pair c overwrites sr[c], already consumed
+        // P~ packed in place: pair c overwrites sr[c], already consumed.  Scalar
+        // arithmetic here: packed pairs of all 128 live scores cost registers.
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
           const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
-          sp[c & 7] += p0 + p1;
+          if (c & 1)
+            sp[(c >> 1) & 3].y += p0 + p1;
+          else
+            sp[(c >> 1) & 3].x += p0 + p1;
           if (DROPOUT) {
             const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
             sr[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
@@ -422,7 +423,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float2 s01 = __fadd2_rn(sp[0], sp[1]);
+      const float2 s23 = __fadd2_rn(sp[2], sp[3]);
+      const float2 s4 = __fadd2_rn(s01, s23);
+      const float sum = s4.x + s4.y;
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       if (!FP8) tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       if (move && j > 0) {
@@ -434,8 +438,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld32(ocol + c * 32, r);
           tmem_ld_wait();
           reg_pin(r);
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          for (int e = 0; e < 16; ++e) {
+            const float2 o2 = __fmul2_rn(
+                make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), a2);
+            r[2 * e] = __float_as_uint(o2.x);
+            r[2 * e + 1] = __float_as_uint(o2.y);
+          }
           tmem_st32(ocol + c * 32, r);
         }
       }

@@ -276,6 +276,28 @@ __device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of the 128 floats held (as bits) in r, as eight interleaved
+// partial maxima of three-input max instructions (short dependency chains).
+__device__ __forceinline__ float row_max128(const uint32_t (&r)[128]) {
+  float mp[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float m = fmax3f(__uint_as_float(r[e]), __uint_as_float(r[e + 8]), __uint_as_float(r[e + 16]));
+#pragma unroll
+    for (int k = 3; k + 1 < 16; k += 2)
+      m = fmax3f(m, __uint_as_float(r[e + 8 * k]), __uint_as_float(r[e + 8 * k + 8]));
+    mp[e] = fmaxf(m, __uint_as_float(r[e + 120]));
+  }
+  return fmax3f(fmax3f(mp[0], mp[1], mp[2]), fmax3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+}
+
 // Four floats to four e4m3 bytes (round to nearest even, saturating to the
 // largest finite e4m3), x0 in the low byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
