@@ -147,13 +147,21 @@ def dist_setup(args):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (timings: the job ends with its slowest rank)."""
     if world == 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(per_rank_work: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank processes the same per-rank work
+    (weak scaling), the job takes as long as its slowest rank."""
+    return world * per_rank_work / seconds_max
 
 
 def barrier(world):
@@ -323,7 +331,7 @@ def run_ours(args, world, rank, local):
     total_ms_max = max_over_ranks(total_ms, world)
     ms_per_step = total_ms_max / args.steps
     f_fwd, f_bwd = flops(w, causal)
-    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_rate(f_fwd + f_bwd, world, ms_per_step * 1e-3) / 1e12
 
     peaks, peak_src = read_peaks()
     long_region = total_ms > 1000.0
@@ -400,7 +408,8 @@ def run_ours(args, world, rank, local):
         plan.close()
         h2d = sum(t.numel() * t.element_size() for t in sets[0][0])
         d2h = sum(t.numel() * t.element_size() for t in sets[0][1])
-        e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": aggregate_rate(f_fwd + f_bwd, world, e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "steps": n_e2e,
                "how": "fa_host_step (C ABI, pinned host buffers, two-slot copy/compute "
@@ -505,7 +514,7 @@ def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
                                      else "", f"dropout p={p_drop}" if p_drop > 0 else "") if x)
         line = {
             "metric": METRIC + f" ({what})",
-            "value": world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "value": aggregate_rate(f_fwd + f_bwd, world, ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": cfg, "fwd_tflops": fwd_tf,
