@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from fa_inputs import WORKLOADS, make_inputs  # noqa: E402
+from fa_inputs import WORKLOADS, make_inputs, sample_indices  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_b2h16n8192d128"
@@ -171,20 +171,48 @@ def barrier(world):
         dist.barrier()
 
 
+ORACLE_FULL_HEAD_MAX_N = 8192  # above this one head's full fp64 step takes too long
+
+
 def oracle_sample(w, causal, q, k, v, dO, bh_index=0):
-    """Time the fp64 oracle (as it stands) on one (batch, head) pair of the
-    workload: full forward and backward.  Returns (seconds, alg_flops, cores)."""
+    """Time the fp64 oracle (as it stands) on a bounded sample of the
+    workload.  Up to N = 8192: the full forward and backward of one (batch,
+    head) pair.  Beyond: 256 seeded query rows of one pair, forward and the
+    row pass of the backward (dq, m, l, D), whose cost per row is what a
+    full run repeats N times per head.  Returns (seconds, flops of what was
+    computed, cores, description, extrapolated seconds of the full problem
+    at the sampled rate or None)."""
     import oracle
 
     b, h = divmod(bh_index % (w.B * w.H), w.H)
     qs, ks, vs, ds = (t[b:b + 1, h:h + 1] for t in (q, k, v, dO))
     cores = oracle.default_threads()
+    if w.N <= ORACLE_FULL_HEAD_MAX_N:
+        t0 = time.perf_counter()
+        oracle.forward(qs, ks, vs, w.scale, causal, nthreads=cores)
+        oracle.backward(qs, ks, vs, ds, w.scale, causal, nthreads=cores)
+        dt = time.perf_counter() - t0
+        base = w.N * w.N * w.d * (0.5 if causal else 1.0)
+        desc = (f"full fp64 forward+backward of 1 of the {w.B * w.H} (batch, head) pairs "
+                f"({dt:.1f} s; flops counted as 14 N^2 d{' x 1/2 causal' if causal else ''} "
+                f"for what the oracle computes)")
+        return dt, 14.0 * base, cores, desc, None
+    rows = sample_indices(w.N, 256, seed=1 + bh_index, must=(0, w.N - 1))
+    visible = sum((i + 1) if causal else w.N for i in rows)
     t0 = time.perf_counter()
-    oracle.forward(qs, ks, vs, w.scale, causal, nthreads=cores)
-    oracle.backward(qs, ks, vs, ds, w.scale, causal, nthreads=cores)
+    oracle.forward(qs, ks, vs, w.scale, causal, rows=rows, nthreads=cores)
+    oracle.backward_rows(qs, ks, vs, ds, w.scale, causal, rows=rows, nthreads=cores)
     dt = time.perf_counter() - t0
-    base = w.N * w.N * w.d * (0.5 if causal else 1.0)
-    return dt, 14.0 * base, cores
+    fl = 12.0 * visible * w.d  # forward 4 n d + row pass 8 n d per row of n visible keys
+    per_row = dt / len(rows)
+    full_rows = w.B * w.H * w.N
+    mean_visible = visible / len(rows)
+    full_visible = w.B * w.H * (w.N * (w.N + 1) / 2 if causal else w.N * w.N)
+    extrap = dt * full_visible / visible * (14.0 / 12.0)
+    desc = (f"256 seeded query rows of 1 of the {w.B * w.H} (batch, head) pairs, fp64 forward "
+            f"+ backward row pass ({dt:.1f} s, {per_row * 1e3:.1f} ms per row of "
+            f"{mean_visible:.0f} visible keys on average; {full_rows} rows in the problem)")
+    return dt, fl, cores, desc, extrap
 
 
 def run_reference(args, world, rank):
@@ -195,14 +223,13 @@ def run_reference(args, world, rank):
     q, k, v, dO = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
     for s in range(args.warmup):
         oracle_sample(w, causal, q, k, v, dO, s)
-    tot_t, tot_f, cores = 0.0, 0.0, 1
+    tot_t, tot_f, cores, desc = 0.0, 0.0, 1, ""
     for s in range(args.steps):
-        dt, fl, cores = oracle_sample(w, causal, q, k, v, dO, args.warmup + s)
+        dt, fl, cores, desc, _ = oracle_sample(w, causal, q, k, v, dO, args.warmup + s)
         tot_t += dt
         tot_f += fl
     value = tot_f / tot_t / 1e12
-    sample = (f"each step: full fp64 forward+backward of one of the {w.B * w.H} (batch, head) "
-              f"pairs (N={w.N}, d={w.d}, {'causal' if causal else 'full'})")
+    sample = f"each step: {desc}"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -313,9 +340,11 @@ def run_ours(args, world, rank, local):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
+    h0 = time.perf_counter()
     for s in range(args.steps):
         evs[s][0].record(stream)
         step(evs[s])
+    enqueue_us = (time.perf_counter() - h0) * 1e6 / args.steps  # host side, per step
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -341,6 +370,18 @@ def run_ours(args, world, rank, local):
     bwd_ms = (per_kernel["bwd_pre"] + per_kernel["bwd_dkdv"] + per_kernel["bwd_dq"]) / args.steps
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    # diagnostics: HBM share of the algorithmic bytes (the measure that matters
+    # for the short, low-intensity workloads), exp2 rate, host enqueue time
+    fwd_bytes, bwd_bytes = alg_bytes(w)
+    diag = {
+        "fwd_hbm_gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9,
+        "fwd_hbm_frac": fwd_bytes / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "bwd_hbm_gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
+        "bwd_hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "fwd_exp2_per_s": w.B * w.H * w.N * w.N * (0.5 if causal else 1.0) / (fwd_ms * 1e-3),
+        "host_enqueue_us_per_step": enqueue_us,
+        "device_us_per_step": ms_per_step * 1e3,
+    }
 
     # dominant kernel and its roofline (algorithmic work of that kernel alone)
     base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
@@ -417,11 +458,11 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, fl, cores = oracle_sample(w, causal, q_h, k_h, v_h, dO_h, 0)
+        dt, fl, cores, desc, extrap = oracle_sample(w, causal, q_h, k_h, v_h, dO_h, 0)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"full fp64 forward+backward of 1 of the {w.B * w.H} (batch, head) "
-                         f"pairs of the workload ({dt:.1f} s; flops counted as 14 N^2 d "
-                         f"{'x 1/2 causal' if causal else ''} for what the oracle computes)"}
+               "sample": desc}
+        if extrap is not None:
+            cpu["extrapolated_full_problem_s"] = extrap
 
     if rank == 0:
         line = {
@@ -432,8 +473,8 @@ def run_ours(args, world, rank, local):
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "fwd_frac_of_peak": fwd_tf / peak, "bwd_frac_of_peak": bwd_tf / peak,
             "peak_tflops": peak, "peak_source": f"{peak_kind} bf16, {peak_src}",
-            "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clk,
+            "kernels": kernels, "roofline": roof, "diagnostics": diag, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     return 0
