@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from fa_inputs import WORKLOADS, make_inputs, sample_indices  # noqa: E402
+from fa_inputs import SCALING_WORKLOADS, WORKLOADS, make_inputs, sample_indices  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_b2h16n8192d128"
@@ -216,7 +216,7 @@ def oracle_sample(w, causal, q, k, v, dO, bh_index=0):
 
 
 def run_reference(args, world, rank):
-    w = WORKLOADS[args.workload]
+    w = {**WORKLOADS, **SCALING_WORKLOADS}[args.workload]
     causal = w.causal[0]
     if rank != 0:
         return 0
@@ -291,7 +291,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = {**WORKLOADS, **SCALING_WORKLOADS}[args.workload]
     causal = w.causal[0] if args.causal is None else bool(args.causal)
     scale = w.scale
     q_h, k_h, v_h, dO_h = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
@@ -700,7 +700,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + sorted(SCALING_WORKLOADS))
     ap.add_argument("--causal", type=int, default=None, help="override the workload's mask mode")
     ap.add_argument("--block-mask", default=None,
                     help="time the block-sparse path with mask band:W[:G] (tiles of 128)")

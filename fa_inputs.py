@@ -58,6 +58,13 @@ WORKLOADS = {
     "short_b64h12n512d64": Workload("short_b64h12n512d64", 64, 12, 512, 64, (False,)),
 }
 
+# The 8K workload's shape at half and twice the sequence length (same B, H,
+# d): the DRAM traffic of every kernel must grow linearly with N.
+SCALING_WORKLOADS = {
+    "causal_b2h16n4096d128": Workload("causal_b2h16n4096d128", 2, 16, 4096, 128, (True,)),
+    "causal_b2h16n16384d128": Workload("causal_b2h16n16384d128", 2, 16, 16384, 128, (True,)),
+}
+
 
 def make_inputs(B: int, H: int, N: int, d: int, seed: int = 0, qk_mult: float = 1.0,
                 with_dO: bool = True):
