@@ -166,6 +166,7 @@ static int forward_impl(const void* q, const void* k, const void* v, void* o, fl
   a.causal = causal ? 1 : 0;
   a.bmask = bmask;
   a.mstride = mstride;
+  a.num_sms = num_sms();
   if (drop) {
     a.dropout = true;
     a.drop = *drop;
@@ -398,6 +399,7 @@ int fa_forward_fp8(const void* q8, const void* k8, const void* vt8, float q_desc
   a.causal = causal ? 1 : 0;
   a.fp8 = true;
   a.o_scale = v_descale;
+  a.num_sms = num_sms();
   cudaError_t e = fa::launch_forward(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -468,6 +470,8 @@ int fa_get_device_error(void* stream, uint32_t* detail) {
   if (fa::fwd_read_clear_error(&w_fwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::bwd_read_clear_error(&w_bwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::dtc_read_clear_error(&w_dtc, s) != cudaSuccess) return FA_ERR_CUDA;
+  // a forward launch that gave up may have left its work-item counters dirty
+  if (w_fwd && fa::fwd_reset_sched(s) != cudaSuccess) return FA_ERR_CUDA;
   const uint32_t w = w_fwd ? w_fwd : (w_bwd ? w_bwd : w_dtc);
   if (detail) *detail = w;
   return w ? FA_ERR_DEVICE_TIMEOUT : FA_OK;

@@ -40,6 +40,8 @@
 // Warp roles (320 threads): warps 0-3 tile 0 and warps 4-7 tile 1
 // (softmax / correction / epilogue; thread t <-> row t <-> TMEM lane t),
 // warp 8 TMA producer, warp 9 TMEM allocator and MMA issuer.
+#include <algorithm>
+#include <mutex>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,10 +56,29 @@ namespace {
 
 __device__ unsigned int g_fwd_error;
 
+// Work-item counters of persistent launches: each launch claims one slot
+// (the host hands them out in turn), its CTAs take items with atomicAdd on
+// slot[0], and the last CTA to finish (slot[1] counts them) zeroes the slot
+// again.  fa_fwd_reset_sched zeroes every slot after a device error, since an
+// aborted launch may leave its slot dirty.
+constexpr int kSchedSlots = 1024;
+__device__ unsigned int g_fwd_sched[kSchedSlots][2];
+constexpr int kItemRing = 4;  // claimed items in flight between the roles of a CTA
+
+
 constexpr int kFwdThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
+
+// Ring slot and phase parity of the K / V tile at ring position pos >= 0
+// (unsigned: kStages is a power of two, so these are a mask and a shift).
+__device__ __forceinline__ int ring_slot(int pos) {
+  return static_cast<int>(static_cast<unsigned>(pos) % kStages);
+}
+__device__ __forceinline__ uint32_t ring_phase(int pos) {
+  return (static_cast<unsigned>(pos) / kStages) & 1u;
+}
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLazyRescaleLog2 = 8.0f;
 
@@ -85,10 +106,14 @@ struct FwdBars {
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_ready[2], pv_done[2];
+  uint64_t q_empty;    // the S products of an item are done with the Q tiles
+  uint64_t item_full[kItemRing];  // the producer has claimed the item of this ring entry
+  uint64_t o_free[2];  // softmax warpgroup g has read its O for the epilogue
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
   int nlist;  // block-sparse: entries of the key-tile list
+  int item_ring[kItemRing];  // claimed items (-1: no more)
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, FwdBars* b,
@@ -115,14 +140,15 @@ __device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity, FwdBars
 // into tensor memory as the A operand of P V, and o_scale (the V descale)
 // multiplies O in the epilogue.  The Q and K descales are folded into
 // scale_log2 by the caller.
-template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8>
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8, bool PERSIST>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int BH, int N, float scale_log2,
                   const uint8_t* __restrict__ bmask, long long mstride, DropArgs drop,
-                  float o_scale) {
+                  float o_scale, unsigned int* __restrict__ sched) {
   static_assert(!FP8 || (D == 128 && !SPARSE && !DROPOUT), "e4m3 path: d = 128, dense");
+  static_assert(!(PERSIST && SPARSE), "block-sparse items each have their own CTA");
   using L = FwdLayout<D, FP8 ? 1 : 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -137,13 +163,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int nq = (N + kTileM - 1) / kTileM;
   const int nk = (N + kTileN - 1) / kTileN;
   const int npairs = (nq + 1) / 2;
-  // head-major order (the query tiles of one head run together and share its
-  // K / V tiles in L2); within a head the heaviest (last) pair first
-  const int pair = npairs - 1 - static_cast<int>(blockIdx.x % npairs);
-  const int bh = static_cast<int>(blockIdx.x / npairs);
+  // Work items: one pair of query tiles of one (b, h).  Head-major order
+  // (the query tiles of one head run together and share its K / V tiles in
+  // L2); within a head the heaviest (last) pair first.  CTA c takes items c,
+  // c + gridDim.x, ...: the launcher makes the grid persistent (one CTA per
+  // SM) for non-causal dense calls and gives every item its own CTA otherwise
+  // (always when SPARSE, whose tile list is built per CTA).
+  const int n_items = BH * npairs;
+  // PERSIST: persistent CTAs (one per SM) claim items in the order above from
+  // the launch's counter slot: the TMA warp claims them and publishes each
+  // through a small ring in shared memory to the MMA warp and the softmax
+  // warpgroups, and the next item's loads and first score product overlap
+  // the current item's epilogue.  Otherwise every item has its own CTA (item
+  // blockIdx.x; block-sparse calls build its tile list before the roles
+  // split).
+  constexpr bool kPersist = PERSIST;
+  auto item_pair = [&](int item) { return npairs - 1 - item % npairs; };
+  auto item_bh = [&](int item) { return item / npairs; };
   // key tiles visited by query tile 2*pair + g
-  const int nkv0 = CAUSAL ? min(2 * pair + 1, nk) : nk;
-  const int nkv1 = CAUSAL ? min(2 * pair + 2, nk) : nk;
+  auto item_nkv = [&](int item, int g) {
+    return CAUSAL ? min(2 * item_pair(item) + 1 + g, nk) : nk;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -157,7 +197,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->p_ready[g], 128);
       mbar_init(&bars->pv_done[g], 1);
+      mbar_init(&bars->o_free[g], 128);
     }
+    mbar_init(&bars->q_empty, 1);
+    for (int r = 0; r < kItemRing; ++r) mbar_init(&bars->item_full[r], 1);
     mbar_init(&bars->drain, 1);
     // an earlier CTA already recorded a pipeline timeout: exit without work
     bars->abort_flag = (*static_cast<volatile unsigned int*>(&g_fwd_error) != 0) ? 1 : 0;
@@ -167,6 +210,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (bars->abort_flag) return;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
   if (SPARSE && warp == 0) {
+    const int pair = item_pair(blockIdx.x), bh = item_bh(blockIdx.x);
     const uint8_t* m0 = bmask + bh * mstride + static_cast<long long>(2 * pair) * nk;
     const bool has1 = 2 * pair + 1 < nq;  // the pair's second tile may lie past N
     int count = 0;
@@ -193,46 +237,89 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
-  // number of list positions each query tile runs through (a prefix of the
-  // pair's list), and the key tile at a position
-  const int n0 = SPARSE ? bars->nlist : nkv0;
-  const int n1 = SPARSE ? bars->nlist : nkv1;
+  // number of list positions each query tile of an item runs through (a
+  // prefix of the pair's list), and the key tile at a position
+  auto item_n = [&](int item, int g) { return SPARSE ? bars->nlist : item_nkv(item, g); };
   auto kv_of = [&](int p) -> int { return SPARSE ? (list[p] & 0x3FFF) : p; };
+  // The t-th item of this CTA as the consumers see it (-1: no more).  `wait`
+  // is the role's bounded wait on the ring entry.
+  auto consumer_item = [&](int t, auto&& wait) -> int {
+    if (!kPersist) return t == 0 ? static_cast<int>(blockIdx.x) : -1;
+    if (!wait(&bars->item_full[t % kItemRing], (t / kItemRing) & 1)) return -1;
+    return bars->item_ring[t % kItemRing];
+  };
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------ TMA producer
-    if (lane == 0 && n1 > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTileBytes);
-#pragma unroll
-      for (int g = 0; g < 2; ++g)
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kQ + g * L::kTileBytes + c * 16384, &tq, &bars->q_full, c * 64,
-                      (2 * pair + g) * kTileM, bh);
-      for (int j = 0; j < n1; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        const int kt = kv_of(j);
-        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x101)) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kK + s * L::kTileBytes + c * 16384, &tk, &bars->k_full[s], c * 64,
-                      kt * kTileN, bh);
-        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x102)) break;
-        mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
-        if (FP8) {  // V^T tile: d rows of 128 keys
-          tma_load_3d(smem + L::kV + s * L::kTileBytes, &tv, &bars->v_full[s], kt * kTileN, 0,
-                      bh);
+      int kvb = 0;  // K / V tiles loaded for earlier items (ring position)
+      bool ok = true;
+      for (int t = 0; ok; ++t) {
+        // claim the next item and publish it to the other roles
+        int item;
+        if (kPersist) {
+          const unsigned int c = atomicAdd(&sched[0], 1u);
+          item = c < static_cast<unsigned int>(n_items) ? static_cast<int>(c) : -1;
+          bars->item_ring[t % kItemRing] = item;
+          mbar_arrive(&bars->item_full[t % kItemRing]);
         } else {
+          item = t == 0 ? static_cast<int>(blockIdx.x) : -1;
+        }
+        if (item < 0) break;
+        const int pair = item_pair(item), bh = item_bh(item);
+        const int n1 = item_n(item, 1);
+        auto load_q = [&]() {
+          mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTileBytes);
+#pragma unroll
+          for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(smem + L::kQ + g * L::kTileBytes + c * 16384, &tq, &bars->q_full,
+                          c * 64, (2 * pair + g) * kTileM, bh);
+        };
+        // a CTA's first item: Q right away; later items: the first K tile
+        // first (its ring slot is free early), then Q once the previous item's
+        // score products are done with the Q buffer
+        if (t == 0 && n1 > 0) load_q();
+        for (int j = 0; j < n1; ++j) {
+          const int s = ring_slot(kvb + j);
+          const uint32_t ph = ring_phase(kvb + j);
+          const int kt = kv_of(j);
+          if (!mbar_wait(&bars->k_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x101)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s],
+            tma_load_3d(smem + L::kK + s * L::kTileBytes + c * 16384, &tk, &bars->k_full[s],
                         c * 64, kt * kTileN, bh);
+          if (j == 0 && t > 0) {
+            if (!mbar_wait(&bars->q_empty, (t - 1) & 1, &bars->abort_flag, &g_fwd_error, 0x103)) {
+              ok = false;
+              break;
+            }
+            load_q();
+          }
+          if (!mbar_wait(&bars->v_empty[s], ph ^ 1, &bars->abort_flag, &g_fwd_error, 0x102)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+          if (FP8) {  // V^T tile: d rows of 128 keys
+            tma_load_3d(smem + L::kV + s * L::kTileBytes, &tv, &bars->v_full[s], kt * kTileN, 0,
+                        bh);
+          } else {
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(smem + L::kV + s * L::kTileBytes + c * 16384, &tv, &bars->v_full[s],
+                          c * 64, kt * kTileN, bh);
+          }
         }
+        kvb += n1;
       }
     }
     __syncwarp();
@@ -242,8 +329,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       constexpr uint32_t idesc_f8 = idesc_e4m3_f32(128, 128);
-      auto issue_s = [&](int g, int j) {
-        const uint32_t kbase = sK + (j % kStages) * L::kTileBytes;
+      // S_g = Q_g K^T from the K tile at ring position pos
+      auto issue_s = [&](int g, int pos) {
+        const uint32_t kbase = sK + ring_slot(pos) * L::kTileBytes;
         const uint32_t qbase = sQ + g * L::kTileBytes;
         if (FP8) {  // K = 32 e4m3 = 32 bytes per instruction, one 128-byte chunk
 #pragma unroll
@@ -260,66 +348,94 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         umma_commit(&bars->s_full[g]);
       };
-      auto issue_pv = [&](int g, int j) {
-        const uint32_t vbase = sV + (j % kStages) * L::kTileBytes;
+      // O_g (+)= P_g V from the V tile at ring position pos; `first` starts O afresh
+      auto issue_pv = [&](int g, int pos, bool first) {
+        const uint32_t vbase = sV + ring_slot(pos) * L::kTileBytes;
         if (FP8) {  // A = P~ e4m3, 8 tensor-memory columns per 32 keys; B = V^T K-major
 #pragma unroll
           for (int kk = 0; kk < kTileN / 32; ++kk)
             umma_ts_f8(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
                        sdesc_sw128(vbase + kk * 32, 16, 1024), idesc_f8,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+                       (!first || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
             umma_ts(tmem + L::o_col(g), tmem + L::s_col(g) + kk * 8,
                     sdesc_sw128(vbase + kk * 2048, 16384, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+                    (!first || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars->pv_done[g]);
       };
-      bool ok = n1 > 0 && mma_wait(&bars->q_full, 0, bars, 0x201) &&
-                mma_wait(&bars->k_full[0], 0, bars, 0x202);
-      tc_fence_after_sync();
-      if (ok) {
-        issue_s(0, 0);
-        issue_s(1, 0);
-        umma_commit(&bars->k_empty[0]);
-      }
-      for (int j = 0; ok && j < n1; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        const int sn = (j + 1) % kStages;
-        const uint32_t phn = ((j + 1) / kStages) & 1;
-        bool v_ready = false, k_next_ready = false;
-        if (j < n0) {
-          ok = mma_wait(&bars->p_ready[0], j & 1, bars, 0x203) &&
-               mma_wait(&bars->v_full[s], ph, bars, 0x204);
-          if (!ok) break;
-          v_ready = true;
-          tc_fence_after_sync();
-          issue_pv(0, j);
-          if (j + 1 < n0) {
-            if (!mma_wait(&bars->k_full[sn], phn, bars, 0x205)) { ok = false; break; }
-            k_next_ready = true;
-            tc_fence_after_sync();
-            issue_s(0, j + 1);
-          }
-        }
-        ok = mma_wait(&bars->p_ready[1], j & 1, bars, 0x206) &&
-             (v_ready || mma_wait(&bars->v_full[s], ph, bars, 0x207));
-        if (!ok) break;
+      // one item: t = items before it in this CTA, kvb = its first K / V ring
+      // position, base0 / base1 = tiles each softmax warpgroup finished before
+      // it.  Returns false after a pipeline timeout.
+      auto mma_item = [&](const int item, const int t, const int kvb, const int base0,
+                          const int base1) -> bool {
+        const int n0 = item_n(item, 0), n1 = item_n(item, 1);
+        if (n1 == 0) return true;  // block-sparse item without key tiles (its only item)
+        bool ok = mma_wait(&bars->q_full, t & 1, bars, 0x201) &&
+             mma_wait(&bars->k_full[ring_slot(kvb)], ring_phase(kvb), bars, 0x202);
+        if (!ok) return false;
         tc_fence_after_sync();
-        issue_pv(1, j);
-        umma_commit(&bars->v_empty[s]);
-        if (j + 1 < n1) {
-          if (!k_next_ready && !mma_wait(&bars->k_full[sn], phn, bars, 0x208)) {
-            ok = false;
-            break;
+        issue_s(0, kvb);
+        issue_s(1, kvb);
+        umma_commit(&bars->k_empty[ring_slot(kvb)]);
+        for (int j = 0; j < n1; ++j) {
+          const int pos = kvb + j;
+          const int s = ring_slot(pos);
+          const uint32_t ph = ring_phase(pos);
+          const int sn = ring_slot(pos + 1);
+          const uint32_t phn = ring_phase(pos + 1);
+          bool v_ready = false, k_next_ready = false;
+          if (j < n0) {
+            ok = mma_wait(&bars->p_ready[0], (base0 + j) & 1, bars, 0x203) &&
+                 mma_wait(&bars->v_full[s], ph, bars, 0x204) &&
+                 (j > 0 || t == 0 || mma_wait(&bars->o_free[0], (t - 1) & 1, bars, 0x209));
+            if (!ok) break;
+            v_ready = true;
+            tc_fence_after_sync();
+            issue_pv(0, pos, j == 0);
+            if (j + 1 < n0) {
+              if (!mma_wait(&bars->k_full[sn], phn, bars, 0x205)) { ok = false; break; }
+              k_next_ready = true;
+              tc_fence_after_sync();
+              issue_s(0, pos + 1);
+            }
           }
+          ok = mma_wait(&bars->p_ready[1], (base1 + j) & 1, bars, 0x206) &&
+               (v_ready || mma_wait(&bars->v_full[s], ph, bars, 0x207)) &&
+               (j > 0 || t == 0 || mma_wait(&bars->o_free[1], (t - 1) & 1, bars, 0x20a));
+          if (!ok) break;
           tc_fence_after_sync();
-          issue_s(1, j + 1);
-          umma_commit(&bars->k_empty[sn]);
+          issue_pv(1, pos, j == 0);
+          umma_commit(&bars->v_empty[s]);
+          if (j + 1 < n1) {
+            if (!k_next_ready && !mma_wait(&bars->k_full[sn], phn, bars, 0x208)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_s(1, pos + 1);
+            umma_commit(&bars->k_empty[sn]);
+          }
         }
+        // every score product of the item has been issued: the Q tiles are
+        // free once they complete
+        umma_commit(&bars->q_empty);
+        return ok;
+      };
+      if (kPersist) {
+        auto mwait = [&](uint64_t* bar, uint32_t par) { return mma_wait(bar, par, bars, 0x20b); };
+        int kvb = 0, base0 = 0, base1 = 0;
+        for (int t = 0;; ++t) {
+          const int item = consumer_item(t, mwait);
+          if (item < 0 || !mma_item(item, t, kvb, base0, base1)) break;
+          kvb += item_n(item, 1);
+          base0 += item_n(item, 0);
+          base1 += item_n(item, 1);
+        }
+      } else {
+        mma_item(static_cast<int>(blockIdx.x), 0, 0, 0, 0);
       }
       umma_commit(&bars->drain);
     }
@@ -328,15 +444,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------ softmax warpgroups
     const int g = warp >> 2;           // which query tile of the pair
     const int t = threadIdx.x & 127;   // row within the tile, TMEM lane
-    const int row = (2 * pair + g) * kTileM + t;
-    const int nkv = g ? n1 : n0;
-    const int q0 = (2 * pair + g) * kTileM;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t scol = tmem + lane_off + L::s_col(g);
     const uint32_t ocol = tmem + lane_off + L::o_col(g);
+    // one item of this warpgroup; tb = tiles it finished in earlier items
+    // (barrier phases).  Returns false after a pipeline timeout.
+    auto softmax_item = [&](const int item, const int tb) -> bool {
+    bool ok = true;
+    const int pair = item_pair(item), bh = item_bh(item);
+    const int row = (2 * pair + g) * kTileM + t;
+    const int nkv = item_n(item, g);
+    const int q0 = (2 * pair + g) * kTileM;
     float m_run = -INFINITY;  // running (lazily moved) max of s * scale * log2(e)
     float l_run = 0.0f;
-    bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       // dropout keep bits of this row for the 128 keys of the tile (bit c of
       // kb[c / 32] for key kv0 + c), drawn before the scores are waited for
@@ -349,7 +469,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                   static_cast<uint32_t>(bh)) << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
-      if (!warp_wait(&bars->s_full[g], j & 1, bars, 0x301)) {
+      if (!warp_wait(&bars->s_full[g], (tb + j) & 1, bars, 0x301)) {
         ok = false;
         break;
       }
@@ -463,7 +583,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
         lse[static_cast<size_t>(bh) * N + row] = -INFINITY;
       }
-    } else if (ok && warp_wait(&bars->pv_done[g], (nkv - 1) & 1, bars, 0x303)) {
+    } else if (ok && (ok = warp_wait(&bars->pv_done[g], (tb + nkv - 1) & 1, bars, 0x303))) {
       tc_fence_after_sync();
       // a row with no visible key (block-sparse) has l = 0: O = 0, lse = -inf;
       // with dropout the kept terms carry the factor 1 / (1 - p)
@@ -491,6 +611,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         lse[static_cast<size_t>(bh) * N + row] =
             l_run > 0.0f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     }
+    // O_g has been read: the next item's first P V may overwrite it
+    tc_fence_before_sync();
+    mbar_arrive(&bars->o_free[g]);
+    return ok;
+    };
+    if (kPersist) {
+      auto swait = [&](uint64_t* bar, uint32_t par) { return warp_wait(bar, par, bars, 0x304); };
+      int tb = 0;
+      for (int tt = 0;; ++tt) {
+        const int item = consumer_item(tt, swait);
+        if (item < 0 || !softmax_item(item, tb)) break;
+        tb += item_n(item, g);
+      }
+    } else {
+      softmax_item(static_cast<int>(blockIdx.x), 0);
+    }
   }
 
   // ------------------------------------------------ teardown
@@ -510,31 +646,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::kTmemCols);
   }
+  // the last CTA of a persistent launch leaves its counter slot zeroed
+  if (kPersist && threadIdx.x == 0 && atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+    atomicExch(&sched[0], 0u);
+    atomicExch(&sched[1], 0u);
+  }
 }
 
-template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8 = false>
+// A counter slot of g_fwd_sched for the next persistent launch on the
+// current device (slots are handed out in turn).
+cudaError_t claim_sched_slot(unsigned int** out) {
+  static std::mutex mu;
+  static unsigned int* base[64] = {};  // g_fwd_sched's address per device
+  static unsigned int next_slot = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_fwd_sched)) != cudaSuccess) return e;
+    base[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = base[dev] + 2 * (next_slot++ % kSchedSlots);
+  return cudaSuccess;
+}
+
+template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8 = false, bool PERSIST = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE, DROPOUT, FP8>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, SPARSE, DROPOUT, FP8, PERSIST>;
   constexpr uint32_t smem = FwdLayout<D, FP8 ? 1 : 2>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long nq = (a.N + kTileM - 1) / kTileM;
-  const long long blocks = (nq + 1) / 2 * a.BH;
-  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  const long long items = (nq + 1) / 2 * a.BH;
+  if (items > 0x7fffffffll) return cudaErrorInvalidValue;
+  // Non-causal items all weigh the same: persistent CTAs, one per SM, take
+  // them in turn.  Causal items weigh 3 .. 2 nq - 1 key tiles, and the hardware
+  // block scheduler, handing out the heaviest-first order one item per CTA as
+  // SMs free up, balances them far better than any fixed assignment; block-
+  // sparse items likewise get one CTA each.
+  constexpr bool kPersist = PERSIST;
+  const long long blocks = kPersist ? std::min<long long>(items, a.num_sms) : items;
+  unsigned int* sched = nullptr;
+  if (kPersist) {
+    if (a.num_sms < 1) return cudaErrorInvalidValue;
+    if ((e = claim_sched_slot(&sched)) != cudaSuccess) return e;
+  }
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
-      a.bmask, a.mstride, a.drop, a.o_scale);
+      a.bmask, a.mstride, a.drop, a.o_scale, sched);
   return cudaGetLastError();
 }
 
-template <bool SPARSE, bool DROPOUT>
+template <bool SPARSE, bool DROPOUT, bool PERSIST = false>
 cudaError_t launch_forward_s(const FwdArgs& a, cudaStream_t s) {
   if (a.d == 64)
-    return a.causal ? launch_fwd_t<64, true, SPARSE, DROPOUT>(a, s)
-                    : launch_fwd_t<64, false, SPARSE, DROPOUT>(a, s);
-  return a.causal ? launch_fwd_t<128, true, SPARSE, DROPOUT>(a, s)
-                  : launch_fwd_t<128, false, SPARSE, DROPOUT>(a, s);
+    return a.causal ? launch_fwd_t<64, true, SPARSE, DROPOUT, false, PERSIST>(a, s)
+                    : launch_fwd_t<64, false, SPARSE, DROPOUT, false, PERSIST>(a, s);
+  return a.causal ? launch_fwd_t<128, true, SPARSE, DROPOUT, false, PERSIST>(a, s)
+                  : launch_fwd_t<128, false, SPARSE, DROPOUT, false, PERSIST>(a, s);
 }
+
+// Dense sequences up to this length run persistent CTAs: with few key tiles
+// per item the per-item start-up and epilogue are a large share of the work,
+// and overlapping them pays; longer sequences keep one CTA per item, whose
+// leaner code runs the long key loops faster.
+constexpr int kPersistMaxN = 2048;
 
 }  // namespace
 
@@ -543,9 +722,22 @@ cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
     return a.causal ? launch_fwd_t<128, true, false, false, true>(a, s)
                     : launch_fwd_t<128, false, false, false, true>(a, s);
   }
-  if (a.dropout)
+  const bool persist = !a.bmask && a.N <= kPersistMaxN && a.num_sms > 0;
+  if (a.dropout) {
+    if (persist) return launch_forward_s<false, true, true>(a, s);
     return a.bmask ? launch_forward_s<true, true>(a, s) : launch_forward_s<false, true>(a, s);
+  }
+  if (persist) return launch_forward_s<false, false, true>(a, s);
   return a.bmask ? launch_forward_s<true, false>(a, s) : launch_forward_s<false, false>(a, s);
+}
+
+cudaError_t fwd_reset_sched(cudaStream_t s) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_fwd_sched);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(p, 0, sizeof(g_fwd_sched), s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
 }
 
 cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s) {

@@ -39,6 +39,7 @@ struct FwdArgs {
   DropArgs drop;
   bool fp8 = false;                // e4m3 Q, K and V^T (tv maps V^T [BH][d][N])
   float o_scale = 1.0f;            // e4m3: V descale, applied to O
+  int num_sms = 0;                 // SMs of the device: persistent grid size (0: one CTA per item)
 };
 
 struct BwdArgs {
@@ -109,6 +110,9 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
 
 // Device error words of each kernel translation unit: read-and-clear.
 cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s);
+// Zero the work-item counters of the forward's persistent launches (after a
+// device error, which may have left a slot dirty); synchronises s.
+cudaError_t fwd_reset_sched(cudaStream_t s);
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s);
 cudaError_t dtc_read_clear_error(uint32_t* out, cudaStream_t s);
 
