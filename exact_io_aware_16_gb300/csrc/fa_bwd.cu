@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
                        float scale_log2, const uint8_t* __restrict__ bmask, long long mstride,
-                       DropArgs drop) {
+                       DropArgs drop, int tile_major) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -330,11 +330,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
-  // head-major order (the key tiles of one head run together and share its
-  // Q / dO tiles in L2); within a head, key tile 0 (the heaviest when causal)
-  // first
-  const int bh = static_cast<int>(blockIdx.x / nt);
-  const int kt = static_cast<int>(blockIdx.x % nt);
+  // CTA order.  Head-major: the key tiles of one head run together and share
+  // its streamed Q / dO tiles in L2; within a head key tile 0 (the heaviest
+  // when causal) first.  Tile-major (tile_major != 0, chosen by the launcher
+  // for causal calls whose Q and dO fit in L2 together): the heaviest key
+  // tile of every head first, which the block scheduler turns into
+  // longest-job-first balancing of the SMs.
+  const int bh = static_cast<int>(tile_major ? blockIdx.x % BH : blockIdx.x / nt);
+  const int kt = static_cast<int>(tile_major ? blockIdx.x / BH : blockIdx.x % nt);
   const int k0 = kt * 128;
   const int i_first = CAUSAL ? kt : 0;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
@@ -587,9 +590,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
-  // head-major order; within a head the heaviest (last) query tile first
-  const int bh = static_cast<int>(blockIdx.x / nt);
-  const int qt = nt - 1 - static_cast<int>(blockIdx.x % nt);
+  // Causal: query tile qt visits qt + 1 key tiles, so the CTAs go tile-major,
+  // the heaviest (last) query tile of every head first (longest-job-first
+  // under the block scheduler); non-causal tiles are equal and go head-major.
+  const int bh = static_cast<int>(CAUSAL ? blockIdx.x % BH : blockIdx.x / nt);
+  const int qt = nt - 1 - static_cast<int>(CAUSAL ? blockIdx.x / BH : blockIdx.x % nt);
   const int q0 = qt * 128;
   const int n_dense = CAUSAL ? (qt + 1) : nt;
   constexpr uint32_t kDQ = L::kAcc0;  // dQ~ accumulator
@@ -823,6 +828,13 @@ cudaError_t prep(Kern k, uint32_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
+// Tile-major CTA order for the dK / dV kernel: causal calls whose streamed
+// Q and dO (all heads) take at most half of the 129 MB L2.
+bool dkdv_tile_major(const BwdArgs& a) {
+  const double qdo_bytes = 2.0 * a.BH * static_cast<double>(a.N) * a.d * 2.0;
+  return a.causal && qdo_bytes <= 64.0 * 1024 * 1024;
+}
+
 template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, SPARSE, DROPOUT>;
@@ -834,7 +846,7 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride,
-      a.drop);
+      a.drop, dkdv_tile_major(a) ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -163,12 +163,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int nq = (N + kTileM - 1) / kTileM;
   const int nk = (N + kTileN - 1) / kTileN;
   const int npairs = (nq + 1) / 2;
-  // Work items: one pair of query tiles of one (b, h).  Head-major order
-  // (the query tiles of one head run together and share its K / V tiles in
-  // L2); within a head the heaviest (last) pair first.  CTA c takes items c,
-  // c + gridDim.x, ...: the launcher makes the grid persistent (one CTA per
-  // SM) for non-causal dense calls and gives every item its own CTA otherwise
-  // (always when SPARSE, whose tile list is built per CTA).
+  // Work items: one pair of query tiles of one (b, h), numbered in the order
+  // they are handed out (item_pair / item_bh below).
   const int n_items = BH * npairs;
   // PERSIST: persistent CTAs (one per SM) claim items in the order above from
   // the launch's counter slot: the TMA warp claims them and publishes each
@@ -178,8 +174,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // blockIdx.x; block-sparse calls build its tile list before the roles
   // split).
   constexpr bool kPersist = PERSIST;
-  auto item_pair = [&](int item) { return npairs - 1 - item % npairs; };
-  auto item_bh = [&](int item) { return item / npairs; };
+  // Causal items differ in size (pair p visits 4p + 3 key tiles): they go
+  // pair-major, the heaviest pair of every head first, so that handing them
+  // out in order (the block scheduler, or the persistent CTAs' counter)
+  // balances the SMs like longest-job-first; the forward needs little DRAM
+  // bandwidth, so spreading the working set over all heads costs nothing.
+  // Equal non-causal items go head-major for L2 locality.
+  auto item_pair = [&](int item) {
+    return npairs - 1 - (CAUSAL ? item / BH : item % npairs);
+  };
+  auto item_bh = [&](int item) { return CAUSAL ? item % BH : item / npairs; };
   // key tiles visited by query tile 2*pair + g
   auto item_nkv = [&](int item, int g) {
     return CAUSAL ? min(2 * item_pair(item) + 1 + g, nk) : nk;
