@@ -253,6 +253,7 @@ static int bwd_step(const void* q, const void* k, const void* v, const void* dO,
   a.causal = causal ? 1 : 0;
   a.bmask = bmask;
   a.mstride = mstride;
+  a.num_sms = num_sms();
   if (drop) {
     a.dropout = true;
     a.drop = *drop;
@@ -470,8 +471,9 @@ int fa_get_device_error(void* stream, uint32_t* detail) {
   if (fa::fwd_read_clear_error(&w_fwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::bwd_read_clear_error(&w_bwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::dtc_read_clear_error(&w_dtc, s) != cudaSuccess) return FA_ERR_CUDA;
-  // a forward launch that gave up may have left its work-item counters dirty
+  // a launch that gave up may have left its work-item counters dirty
   if (w_fwd && fa::fwd_reset_sched(s) != cudaSuccess) return FA_ERR_CUDA;
+  if (w_bwd && fa::bwd_reset_sched(s) != cudaSuccess) return FA_ERR_CUDA;
   const uint32_t w = w_fwd ? w_fwd : (w_bwd ? w_bwd : w_dtc);
   if (detail) *detail = w;
   return w ? FA_ERR_DEVICE_TIMEOUT : FA_OK;

@@ -60,6 +60,7 @@ struct BwdArgs {
   long long mstride = 0;
   bool dropout = false;  // dropout on P with the parameters in drop
   DropArgs drop;
+  int num_sms = 0;  // SMs of the device: persistent grid size (0: one CTA per tile)
 };
 
 struct DecodeArgs {
@@ -113,6 +114,7 @@ cudaError_t fwd_read_clear_error(uint32_t* out, cudaStream_t s);
 // Zero the work-item counters of the forward's persistent launches (after a
 // device error, which may have left a slot dirty); synchronises s.
 cudaError_t fwd_reset_sched(cudaStream_t s);
+cudaError_t bwd_reset_sched(cudaStream_t s);
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s);
 cudaError_t dtc_read_clear_error(uint32_t* out, cudaStream_t s);
 
