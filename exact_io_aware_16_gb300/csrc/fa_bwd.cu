@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
                        float scale_log2, const uint8_t* __restrict__ bmask, long long mstride,
-                       DropArgs drop, int tile_major, unsigned int* __restrict__ sched) {
+                       DropArgs drop, int group_heads, unsigned int* __restrict__ sched) {
   static_assert(!(PERSIST && SPARSE), "block-sparse tiles each have their own CTA");
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -390,17 +390,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
   // Work items: one key tile of one (b, h), numbered in the order they are
-  // handed out.  Head-major: the key tiles of one head run together and share
-  // its streamed Q / dO tiles in L2; within a head key tile 0 (the heaviest
-  // when causal) first.  Tile-major (tile_major != 0, chosen by the launcher
-  // for causal calls whose Q and dO fit in L2 together): the heaviest key
-  // tile of every head first, which handing them out in order turns into
-  // longest-job-first balancing of the SMs.  PERSIST: persistent CTAs claim
-  // items from the launch's counter slot (the TMA warp claims, a ring in
-  // shared memory publishes them); otherwise CTA = item blockIdx.x.
+  // handed out: in groups of group_heads heads, tile-major within a group,
+  // key tile 0 (the heaviest when causal) of every head first.  Handing them
+  // out in order balances the SMs like longest-job-first while the Q / dO
+  // tiles a group streams stay within L2 (the launcher sizes the group; 1 =
+  // head-major).  PERSIST: persistent CTAs claim items from the launch's
+  // counter slot (the TMA warp claims, a ring in shared memory publishes
+  // them); otherwise CTA = item blockIdx.x.
   const int n_items = BH * nt;
-  auto item_bh = [&](int item) { return tile_major ? item % BH : item / nt; };
-  auto item_kt = [&](int item) { return tile_major ? item / BH : item % nt; };
+  auto item_rank = [&](int item, int& head) {
+    const int grp = item / (group_heads * nt);
+    const int gs = min(group_heads, BH - grp * group_heads);
+    const int r = item - grp * group_heads * nt;
+    head = grp * group_heads + r % gs;
+    return r / gs;
+  };
+  auto item_bh = [&](int item) {
+    int head;
+    item_rank(item, head);
+    return head;
+  };
+  auto item_kt = [&](int item) {
+    int head;
+    return item_rank(item, head);
+  };
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
   if (SPARSE && warp == 0) {  // column kt of the mask: query tiles i >= i_first
     const int bh = item_bh(blockIdx.x), kt = item_kt(blockIdx.x);
@@ -714,7 +727,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse,
                      float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dq, int BH, int N,
                      float scale, float scale_log2, const uint8_t* __restrict__ bmask,
-                     long long mstride, DropArgs drop, unsigned int* __restrict__ sched) {
+                     long long mstride, DropArgs drop, int group_heads,
+                     unsigned int* __restrict__ sched) {
   static_assert(!(PERSIST && SPARSE), "block-sparse tiles each have their own CTA");
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -726,14 +740,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nt = (N + 127) / 128;
   // Work items: one query tile of one (b, h), numbered in the order they are
-  // handed out.  Causal: query tile qt visits qt + 1 key tiles, so the items
-  // go tile-major, the heaviest (last) query tile of every head first
-  // (longest-job-first balancing); non-causal tiles are equal and go
-  // head-major.  PERSIST: persistent CTAs claim items from the launch's
-  // counter slot; otherwise CTA = item blockIdx.x.
+  // handed out: in groups of group_heads heads, tile-major within a group,
+  // the heaviest (last, qt + 1 key tiles when causal) query tile of every
+  // head first (longest-job-first balancing, with the K / V tiles a group
+  // streams within L2; 1 = head-major).  PERSIST: persistent CTAs claim
+  // items from the launch's counter slot; otherwise CTA = item blockIdx.x.
   const int n_items = BH * nt;
-  auto item_bh = [&](int item) { return CAUSAL ? item % BH : item / nt; };
-  auto item_qt = [&](int item) { return nt - 1 - (CAUSAL ? item / BH : item % nt); };
+  auto item_rank = [&](int item, int& head) {
+    const int grp = item / (group_heads * nt);
+    const int gs = min(group_heads, BH - grp * group_heads);
+    const int r = item - grp * group_heads * nt;
+    head = grp * group_heads + r % gs;
+    return r / gs;
+  };
+  auto item_bh = [&](int item) {
+    int head;
+    item_rank(item, head);
+    return head;
+  };
+  auto item_qt = [&](int item) {
+    int head;
+    return nt - 1 - item_rank(item, head);
+  };
   constexpr uint32_t kDQ = L::kAcc0;  // dQ~ accumulator
   constexpr uint32_t kB = L::kAcc1;   // B = P K accumulator
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
@@ -1038,11 +1066,15 @@ cudaError_t prep(Kern k, uint32_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-// Tile-major CTA order for the dK / dV kernel: causal calls whose streamed
-// Q and dO (all heads) take at most half of the 129 MB L2.
-bool dkdv_tile_major(const BwdArgs& a) {
-  const double qdo_bytes = 2.0 * a.BH * static_cast<double>(a.N) * a.d * 2.0;
-  return a.causal && qdo_bytes <= 64.0 * 1024 * 1024;
+// Heads per group of the tile order (both kernels stream two [N][d] bf16
+// tensors per head): causal calls take as many heads as keep a group's
+// streamed tiles within half of the 129 MB L2; non-causal calls 1
+// (head-major: the tiles are equal).
+int bwd_group_heads(const BwdArgs& a) {
+  if (!a.causal) return 1;
+  const double per_head = 2.0 * a.N * a.d * 2.0;
+  const double g = (64.0 * 1024 * 1024) / per_head;
+  return static_cast<int>(g < 1.0 ? 1.0 : (g > a.BH ? a.BH : g));
 }
 
 // A counter slot of g_bwd_sched for the next persistent launch on the
@@ -1093,7 +1125,7 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   kern<<<blocks, kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride,
-      a.drop, dkdv_tile_major(a) ? 1 : 0, sched);
+      a.drop, bwd_group_heads(a), sched);
   return cudaGetLastError();
 }
 
@@ -1108,7 +1140,7 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
   if ((e = bwd_grid<PERSIST>(a, &blocks, &sched)) != cudaSuccess) return e;
   kern<<<blocks, kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.BH, a.N,
-      a.scale, a.scale_log2, a.bmask, a.mstride, a.drop, sched);
+      a.scale, a.scale_log2, a.bmask, a.mstride, a.drop, bwd_group_heads(a), sched);
   return cudaGetLastError();
 }
 

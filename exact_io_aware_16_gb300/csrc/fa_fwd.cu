@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int BH, int N, float scale_log2,
                   const uint8_t* __restrict__ bmask, long long mstride, DropArgs drop,
-                  float o_scale, unsigned int* __restrict__ sched) {
+                  float o_scale, unsigned int* __restrict__ sched, int group_heads) {
   static_assert(!FP8 || (D == 128 && !SPARSE && !DROPOUT), "e4m3 path: d = 128, dense");
   static_assert(!(PERSIST && SPARSE), "block-sparse items each have their own CTA");
   using L = FwdLayout<D, FP8 ? 1 : 2>;
@@ -174,16 +174,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // blockIdx.x; block-sparse calls build its tile list before the roles
   // split).
   constexpr bool kPersist = PERSIST;
-  // Causal items differ in size (pair p visits 4p + 3 key tiles): they go
-  // pair-major, the heaviest pair of every head first, so that handing them
-  // out in order (the block scheduler, or the persistent CTAs' counter)
-  // balances the SMs like longest-job-first; the forward needs little DRAM
-  // bandwidth, so spreading the working set over all heads costs nothing.
-  // Equal non-causal items go head-major for L2 locality.
-  auto item_pair = [&](int item) {
-    return npairs - 1 - (CAUSAL ? item / BH : item % npairs);
+  // Items come in groups of group_heads heads (all pairs of those heads);
+  // within a group pair-major, the heaviest pair (4p + 3 key tiles when
+  // causal) of every head first.  Handing them out in order (the block
+  // scheduler, or the persistent CTAs' counter) then balances the SMs like
+  // longest-job-first, while the K / V tiles a group reads at once stay
+  // within L2 (the launcher sizes the group; 1 = head-major, for the equal
+  // non-causal items).
+  auto item_group = [&](int item) { return item / (group_heads * npairs); };
+  auto item_rank = [&](int item, int& head) {  // rank of the pair in its group, heaviest first
+    const int grp = item_group(item);
+    const int gs = min(group_heads, BH - grp * group_heads);
+    const int r = item - grp * group_heads * npairs;
+    head = grp * group_heads + r % gs;
+    return r / gs;
   };
-  auto item_bh = [&](int item) { return CAUSAL ? item % BH : item / npairs; };
+  auto item_pair = [&](int item) {
+    int head;
+    return npairs - 1 - item_rank(item, head);
+  };
+  auto item_bh = [&](int item) {
+    int head;
+    item_rank(item, head);
+    return head;
+  };
   // key tiles visited by query tile 2*pair + g
   auto item_nkv = [&](int item, int g) {
     return CAUSAL ? min(2 * item_pair(item) + 1 + g, nk) : nk;
@@ -657,6 +671,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+// Heads per group of the item order: causal calls take as many heads as keep
+// the K / V tiles of a group within half of the 129 MB L2 (the pairs of a
+// group go heaviest first across its heads); non-causal calls 1 (head-major).
+int group_heads(const FwdArgs& a) {
+  if (!a.causal) return 1;
+  const double kv_head = 2.0 * a.N * a.d * (a.fp8 ? 1.0 : 2.0);
+  const double g = (64.0 * 1024 * 1024) / kv_head;
+  return static_cast<int>(g < 1.0 ? 1.0 : (g > a.BH ? a.BH : g));
+}
+
 // A counter slot of g_fwd_sched for the next persistent launch on the
 // current device (slots are handed out in turn).
 cudaError_t claim_sched_slot(unsigned int** out) {
@@ -700,7 +724,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   }
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
-      a.bmask, a.mstride, a.drop, a.o_scale, sched);
+      a.bmask, a.mstride, a.drop, a.o_scale, sched, group_heads(a));
   return cudaGetLastError();
 }
 
