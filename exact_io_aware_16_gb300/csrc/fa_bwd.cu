@@ -337,26 +337,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&w)[16]
       : "memory");
 }
 
-// Store 64 fp32 accumulator columns [addr, addr+64) of this lane as bf16
-// (times `mul`) to 64 consecutive elements at dst.
-__device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bfloat16* dst,
-                                               bool valid) {
+// Store 64 fp32 accumulator columns [addr, addr+64) of this lane's row as bf16
+// (times `mul`), written together with the rows of this lane's 8-lane group:
+// grp_dst / ld / grp_rows as for store_rows.
+__device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bfloat16* grp_dst,
+                                               long long ld, int grp_rows) {
+  uint32_t w[32];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t r[32];
     tmem_ld32(addr + c * 32, r);
     tmem_ld_wait();
     reg_pin(r);
-    uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e)
-      w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-    if (valid) {
-      uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-    }
+      w[16 * c + e] =
+          pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
   }
+  store_rows<8>(w, grp_dst, ld, grp_rows);
 }
 
 // ============================================================ dK / dV
@@ -673,18 +671,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else if (ok && (ok = bwd_warp_wait(&bars->acc_done, t & 1, bars, 0x302))) {
       tc_fence_after_sync();
-      const bool valid = krow < N;
-      const size_t off = (static_cast<size_t>(bh) * N + (valid ? krow : 0)) * D;
+      // rows of this lane's 8-lane group (stored together, row by row)
+      const int r0 = krow - (lane & 7);
+      const int grp_rows = min(8, N - r0);
+      const size_t off = (static_cast<size_t>(bh) * N + (grp_rows > 0 ? r0 : 0)) * D;
       // d = 128: warpgroup g stores columns [64g, 64g+64) of dV and dK;
       // d = 64: warpgroup 0 stores dV, warpgroup 1 stores dK
       const float dv_mul = DROPOUT ? drop.rs : 1.0f;
       if (D == 128) {
-        store_acc_half(tmem + lane_off + L::kAcc0 + col0, dv_mul, dv + off + col0, valid);
-        store_acc_half(tmem + lane_off + L::kAcc1 + col0, scale, dk + off + col0, valid);
+        store_acc_half(tmem + lane_off + L::kAcc0 + col0, dv_mul, dv + off + col0, D, grp_rows);
+        store_acc_half(tmem + lane_off + L::kAcc1 + col0, scale, dk + off + col0, D, grp_rows);
       } else if (g == 0) {
-        store_acc_half(tmem + lane_off + L::kAcc0, dv_mul, dv + off, valid);
+        store_acc_half(tmem + lane_off + L::kAcc0, dv_mul, dv + off, D, grp_rows);
       } else {
-        store_acc_half(tmem + lane_off + L::kAcc1, scale, dk + off, valid);
+        store_acc_half(tmem + lane_off + L::kAcc1, scale, dk + off, D, grp_rows);
       }
     }
     // the accumulators have been read: the next item may overwrite them
@@ -1009,11 +1009,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       const float Dfull = dx_s[tr] + dx_s[128 + tr];
       const float corr = Dfull - Dt;
-      const size_t off = (static_cast<size_t>(bh) * N + (rvalid ? row : 0)) * D;
+      // rows of this lane's 8-lane group (stored together, row by row)
+      const int r0 = row - (lane & 7);
+      const int grp_rows = min(8, N - r0);
+      const size_t off = (static_cast<size_t>(bh) * N + (grp_rows > 0 ? r0 : 0)) * D;
       // d = 128: warpgroup g stores dq columns [64g, 64g+64); d = 64: warpgroup 0 only
       if (D == 128 || g == 0) {
         const uint32_t c0 = (D == 128) ? col0 : 0u;
-        __nv_bfloat16* dst = dq + off + c0;
+        uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t a[32], b[32];
@@ -1022,22 +1025,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
           reg_pin(a);
           reg_pin(b);
-          uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float x0 =
                 scale * fmaf(-corr, __uint_as_float(b[2 * e]), __uint_as_float(a[2 * e]));
             const float x1 =
                 scale * fmaf(-corr, __uint_as_float(b[2 * e + 1]), __uint_as_float(a[2 * e + 1]));
-            w[e] = pack_bf16x2(x0, x1);
-          }
-          if (rvalid) {
-            uint4* p = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              p[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            w[16 * c + e] = pack_bf16x2(x0, x1);
           }
         }
+        store_rows<8>(w, dq + off + c0, D, grp_rows);
       }
       if (g == 0 && rvalid) Dvec[static_cast<size_t>(bh) * N + row] = Dfull;
     }

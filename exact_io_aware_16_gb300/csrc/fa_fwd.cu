@@ -607,7 +607,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // with dropout the kept terms carry the factor 1 / (1 - p)
       const float inv_l =
           l_run > 0.0f ? (DROPOUT ? drop.rs : 1.0f) * (FP8 ? o_scale : 1.0f) / l_run : 0.0f;
-      __nv_bfloat16* orow = o + (static_cast<size_t>(bh) * N + row) * D;
+      // Rows of this lane's 4-lane group are stored together, row by row (32
+      // columns at a time: the softmax warps' registers are scarce).  The
+      // persistent causal kernel, which carries its item state across the
+      // epilogue, has no registers left for the transpose and stores its own
+      // row (measured: the transpose there spills and costs 7 % at N = 2048).
+      constexpr bool kGroupStore = !(PERSIST && CAUSAL);
+      const int r0 = kGroupStore ? row - (lane & 3) : row;
+      const int grp_rows = min(kGroupStore ? 4 : 1, N - r0);
+      __nv_bfloat16* ogrp = o + (static_cast<size_t>(bh) * N + (grp_rows > 0 ? r0 : 0)) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -618,8 +626,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-        if (row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        if (kGroupStore) {
+          store_rows<4>(w, ogrp + c * 32, D, grp_rows);
+        } else if (grp_rows > 0) {
+          uint4* dst = reinterpret_cast<uint4*>(ogrp + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);

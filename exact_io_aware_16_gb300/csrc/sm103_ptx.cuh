@@ -329,6 +329,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---------------------------------------------------------------- row stores
+// Epilogues hold one output row per thread (the TMEM lane).  Storing that
+// way, every 16-byte store of a warp lands in 32 different rows; instead the
+// G lanes of each group (rows r0 .. r0+G-1, r0 = row - lane % G) first
+// transpose their 16-byte chunks so that lane r0 + a holds chunk a of all G
+// rows, and then G stores each write one row's 16 G contiguous bytes with G
+// lanes (G = 8: whole 128-byte lines).
+//
+// w: this lane's 8 G bf16 (chunk j = w[4j .. 4j+3], columns 8j .. 8j+7).
+// After the call chunk slot k holds chunk (lane % G) of row r0 + k.  All 32
+// lanes of the warp must call it together.
+template <int G>
+__device__ __forceinline__ void transpose_chunks(uint32_t (&w)[4 * G]) {
+  static_assert(G == 4 || G == 8, "groups of 4 or 8 lanes");
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 1; s < G; s <<= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      if (j & s) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // the lower lane of the pair passes on its chunk j^s and takes the
+        // partner's chunk j into slot j^s; the upper lane the other way round
+        const uint32_t send = upper ? w[4 * j + e] : w[4 * (j ^ s) + e];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
+        if (upper)
+          w[4 * j + e] = recv;
+        else
+          w[4 * (j ^ s) + e] = recv;
+      }
+    }
+  }
+}
+
+// Stores the 8 G bf16 of w (this lane's row segment) as described above.
+// grp_dst: element address of the segment's first column in row r0 of this
+// lane's group; ld: elements between rows; grp_rows: rows r0 .. r0+grp_rows-1
+// exist (nothing is stored for the others; grp_dst is not dereferenced when
+// grp_rows <= 0).
+template <int G>
+__device__ __forceinline__ void store_rows(uint32_t (&w)[4 * G], __nv_bfloat16* grp_dst,
+                                           long long ld, int grp_rows) {
+  transpose_chunks<G>(w);
+  const int a = threadIdx.x & (G - 1);
+#pragma unroll
+  for (int k = 0; k < G; ++k)
+    if (k < grp_rows)
+      *reinterpret_cast<uint4*>(grp_dst + k * ld + a * 8) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
 // Named barrier among `nthreads` threads (a multiple of 32) of this CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
