@@ -132,6 +132,14 @@ struct BwdBars {
   int item_ring[kItemRing];  // claimed items (-1: no more)
 };
 
+// Adds `bytes` to the transaction count of the current phase of `bar`
+// without arriving (the arrival comes separately, after staged data).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Ring slot and phase parity of the streamed tile at ring position pos >= 0.
 __device__ __forceinline__ int ring_slot(int pos) {
   return static_cast<int>(static_cast<unsigned>(pos) % kStages);
@@ -249,6 +257,18 @@ __device__ __forceinline__ bool bwd_producer_item(uint8_t* smem, BwdBars* bars,
     bool ok = mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101);
     if (!__all_sync(0xffffffffu, ok)) return false;
     const int row0 = (list ? static_cast<int>(list[n]) : first_tile + n) * 128;
+    // the tiles first, then (while they are in flight) the staged vectors; the
+    // stage's one arrival comes last, after both
+    if (lane == 0) {
+      mbar_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s],
+                    c * 64, row0, bh);
+        tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s],
+                    c * 64, row0, bh);
+      }
+    }
     if (lse_bh != nullptr) {
       float* vec = reinterpret_cast<float*>(smem + L::kVec) + s * 256;  // [lse2 | D]
 #pragma unroll
@@ -258,18 +278,9 @@ __device__ __forceinline__ bool bwd_producer_item(uint8_t* smem, BwdBars* bars,
         vec[i] = (q < N) ? lse_bh[q] * kLog2e : INFINITY;
         vec[128 + i] = (q < N) ? D_bh[q] : 0.0f;
       }
-      __syncwarp();
     }
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s],
-                    c * 64, row0, bh);
-        tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s],
-                    c * 64, row0, bh);
-      }
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->str_full[s]);
     __syncwarp();
     if (n == 0 && t > 0) {
       ok = mbar_wait(&bars->res_empty, (t - 1) & 1, &bars->abort_flag, &g_bwd_error, 0x102);
