@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -599,20 +600,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P^T for this key row and query columns [col0, col0+64)
       uint32_t pr[64];
       tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
+      // only the diagonal tile needs the causal mask (query rows past N have
+      // lse = +inf staged, so their P is 0 without one); the test is uniform
+      // across the warp
       const bool diag = CAUSAL && (it == kt);
       const float4* lse4 = reinterpret_cast<const float4*>(lse2_s + col0);
+      auto exp_cols = [&](auto masked) {
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = lse4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = lse4[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lv[e]));
-          if (diag && (q0 + static_cast<int>(col0) + c < krow)) p = 0.0f;  // query before key
-          pr[c] = __float_as_uint(p);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lv[e]));
+            if (masked && (q0 + static_cast<int>(col0) + c < krow)) p = 0.0f;  // query before key
+            pr[c] = __float_as_uint(p);
+          }
         }
-      }
+      };
+      if (diag)
+        exp_cols(std::true_type{});
+      else
+        exp_cols(std::false_type{});
       {
         uint32_t pk[32];
 #pragma unroll
@@ -945,15 +955,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pr[64];
       tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
       const int kv0 = kt_of(n) * 128;
+      // only the diagonal tile (causal) and a ragged last tile need a mask:
+      // the test is uniform across the warp, so other tiles skip it
       const bool need_mask = (CAUSAL && kv0 + 127 > q0) || (kv0 + 128 > N);
-      const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
-      const int lim_n = N - 1 - kv0;
-      const int lim = need_mask ? (lim_c < lim_n ? lim_c : lim_n) : 0x7fffffff;
+      if (need_mask) {
+        const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
+        const int lim_n = N - 1 - kv0;
+        const int lim = (lim_c < lim_n ? lim_c : lim_n) - static_cast<int>(col0);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2));
-        if (static_cast<int>(col0) + c > lim) p = 0.0f;
-        pr[c] = __float_as_uint(p);
+        for (int c = 0; c < 64; ++c) {
+          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2));
+          if (c > lim) p = 0.0f;
+          pr[c] = __float_as_uint(p);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          pr[c] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2)));
       }
       {
         uint32_t pk[32];
