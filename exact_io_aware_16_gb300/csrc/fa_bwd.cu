@@ -605,17 +605,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // across the warp
       const bool diag = CAUSAL && (it == kt);
       const float4* lse4 = reinterpret_cast<const float4*>(lse2_s + col0);
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
       auto exp_cols = [&](auto masked) {
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l4 = lse4[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lv[e]));
-            if (masked && (q0 + static_cast<int>(col0) + c < krow)) p = 0.0f;  // query before key
-            pr[c] = __float_as_uint(p);
+          for (int h = 0; h < 2; ++h) {  // two columns per packed fma
+            const int c = 4 * c4 + 2 * h;
+            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])), sc2, nl);
+            float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            if (masked) {  // query before key
+              if (q0 + static_cast<int>(col0) + c < krow) p0 = 0.0f;
+              if (q0 + static_cast<int>(col0) + c + 1 < krow) p1 = 0.0f;
+            }
+            pr[c] = __float_as_uint(p0);
+            pr[c + 1] = __float_as_uint(p1);
           }
         }
       };
@@ -665,12 +672,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) dp[e] = ((bits >> e) & 1u) ? dp[e] * drop.rs : 0.0f;
           }
-          const float ds0 = __uint_as_float(pr[c]) * (dp[0] - dd.x);
-          const float ds1 = __uint_as_float(pr[c + 1]) * (dp[1] - dd.y);
-          const float ds2 = __uint_as_float(pr[c + 2]) * (dp[2] - dd.z);
-          const float ds3 = __uint_as_float(pr[c + 3]) * (dp[3] - dd.w);
-          w[2 * e4] = pack_bf16x2(ds0, ds1);
-          w[2 * e4 + 1] = pack_bf16x2(ds2, ds3);
+          // dS^T = P^T (dP^T - D), two columns per packed op (each lane
+          // rounded as the scalar ops)
+          const float2 ds01 = __fmul2_rn(
+              make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])),
+              __fadd2_rn(make_float2(dp[0], dp[1]), make_float2(-dd.x, -dd.y)));
+          const float2 ds23 = __fmul2_rn(
+              make_float2(__uint_as_float(pr[c + 2]), __uint_as_float(pr[c + 3])),
+              __fadd2_rn(make_float2(dp[2], dp[3]), make_float2(-dd.z, -dd.w)));
+          w[2 * e4] = pack_bf16x2(ds01.x, ds01.y);
+          w[2 * e4 + 1] = pack_bf16x2(ds23.x, ds23.y);
         }
         tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
       }
@@ -933,7 +944,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool rvalid = row < N;
     const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
     const float Dt = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;  // D~
-    float dxp[4] = {0.f, 0.f, 0.f, 0.f};  // this half's part of the exact D = sum_j P_ij dP_ij
+    // this half's part of the exact D = sum_j P_ij dP_ij (four partial sums)
+    float2 dx2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     bool ok = true;
     for (int n = 0; n < n_iters; ++n) {
       // dropout keep bits of this row for keys kt_of(n) * 128 + col0 + c
@@ -958,20 +970,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // only the diagonal tile (causal) and a ragged last tile need a mask:
       // the test is uniform across the warp, so other tiles skip it
       const bool need_mask = (CAUSAL && kv0 + 127 > q0) || (kv0 + 128 > N);
+      // exponent argument s * scale * log2(e) - lse * log2(e), two columns
+      // per packed fma (each lane rounded as the scalar fma)
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nl2 = make_float2(-lse2, -lse2);
+      auto exp_cols = [&](auto masked, int lim) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x =
+              __ffma2_rn(make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])), sc2, nl2);
+          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          if (masked) {
+            if (c > lim) p0 = 0.0f;
+            if (c + 1 > lim) p1 = 0.0f;
+          }
+          pr[c] = __float_as_uint(p0);
+          pr[c + 1] = __float_as_uint(p1);
+        }
+      };
       if (need_mask) {
         const int lim_c = CAUSAL ? (row - kv0) : 0x7fffffff;
         const int lim_n = N - 1 - kv0;
-        const int lim = (lim_c < lim_n ? lim_c : lim_n) - static_cast<int>(col0);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2));
-          if (c > lim) p = 0.0f;
-          pr[c] = __float_as_uint(p);
-        }
+        exp_cols(std::true_type{}, (lim_c < lim_n ? lim_c : lim_n) - static_cast<int>(col0));
       } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          pr[c] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(pr[c]), scale_log2, -lse2)));
+        exp_cols(std::false_type{}, 0);
       }
       {
         uint32_t pk[32];
@@ -988,6 +1010,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
+      const float2 nD2 = make_float2(-Dt, -Dt);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t r[32];
@@ -998,16 +1021,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = c2 * 32 + 2 * e;
-          const float p0 = __uint_as_float(pr[c]), p1 = __uint_as_float(pr[c + 1]);
-          float dp0 = __uint_as_float(r[2 * e]), dp1 = __uint_as_float(r[2 * e + 1]);
+          const float2 pp = make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1]));
+          float2 dd = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
           if (DROPOUT) {  // dP of the dropped product: rs Z o (dO V^T)
             const uint32_t bits = kb[c >> 5] >> (c & 31);
-            dp0 = (bits & 1u) ? dp0 * drop.rs : 0.0f;
-            dp1 = (bits & 2u) ? dp1 * drop.rs : 0.0f;
+            dd.x = (bits & 1u) ? dd.x * drop.rs : 0.0f;
+            dd.y = (bits & 2u) ? dd.y * drop.rs : 0.0f;
           }
-          dxp[(2 * e) & 3] = fmaf(p0, dp0, dxp[(2 * e) & 3]);
-          dxp[(2 * e + 1) & 3] = fmaf(p1, dp1, dxp[(2 * e + 1) & 3]);
-          w[e] = pack_bf16x2(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
+          // exact D: columns 2e and 2e + 1 feed partial sums (e & 1) x / y;
+          // dS = P (dP - D~), packed (each lane rounded as the scalar ops)
+          dx2[e & 1] = __ffma2_rn(pp, dd, dx2[e & 1]);
+          const float2 ds = __fmul2_rn(pp, __fadd2_rn(dd, nD2));
+          w[e] = pack_bf16x2(ds.x, ds.y);
         }
         tmem_st16(tmem + lane_off + L::kDPCol + col0 + c2 * 16, w);
       }
@@ -1030,7 +1055,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // alternates between items
     float* dx_s = dx_base + (t & 1) * 256;
     if (ok) {
-      dx_s[g * 128 + tr] = (dxp[0] + dxp[1]) + (dxp[2] + dxp[3]);
+      dx_s[g * 128 + tr] = (dx2[0].x + dx2[0].y) + (dx2[1].x + dx2[1].y);
       mbar_arrive(&bars->dx_ready);
       ok = bwd_warp_wait(&bars->dx_ready, t & 1, bars, 0x313);
     }
