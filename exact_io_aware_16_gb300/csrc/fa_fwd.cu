@@ -543,21 +543,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           sr[c] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
         }
       } else {
-        // P~ packed in place: pair c overwrites sr[c], already consumed.  Scalar
-        // arithmetic here: packed pairs of all 128 live scores cost registers.
+        // P~ packed in place: pair c overwrites sr[c], already consumed.  The
+        // row sum adds each pair (p0 + p1) into partial sum (c / 2) % 4, x for
+        // even c and y for odd c.  Two pairs at a time, with packed fma / add
+        // (each lane rounded as the scalar op, so the sums are the same bit
+        // for bit), except in the dropout kernels and the persistent causal
+        // d = 128 kernel, whose generator or item state leaves no registers
+        // for them (they spilled; the latter ran 8 % slower at N = 2048).
+        constexpr bool kPairs = !DROPOUT && !(PERSIST && CAUSAL && D == 128);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_use));
-          if (c & 1)
-            sp[(c >> 1) & 3].y += p0 + p1;
-          else
-            sp[(c >> 1) & 3].x += p0 + p1;
-          if (DROPOUT) {
-            const uint32_t bits = kb[c >> 4] >> ((2 * c) & 31);
-            sr[c] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+        for (int c = 0; c < 64; c += 2) {
+          float p[4];
+          if (kPairs) {
+            const float2 x0 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+            const float2 x1 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[2 * c + 2]), __uint_as_float(sr[2 * c + 3])), sc2,
+                nm2);
+            p[0] = ex2_approx(x0.x);
+            p[1] = ex2_approx(x0.y);
+            p[2] = ex2_approx(x1.x);
+            p[3] = ex2_approx(x1.y);
+            const float2 pair = __fadd2_rn(make_float2(p[0], p[2]), make_float2(p[1], p[3]));
+            sp[(c >> 1) & 3] = __fadd2_rn(sp[(c >> 1) & 3], pair);
           } else {
-            sr[c] = pack_bf16x2(p0, p1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              p[e] = ex2_approx(fmaf(__uint_as_float(sr[2 * c + e]), scale_log2, -m_use));
+            sp[(c >> 1) & 3].x += p[0] + p[1];
+            sp[(c >> 1) & 3].y += p[2] + p[3];
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float p0 = p[2 * h], p1 = p[2 * h + 1];
+            const int cc = c + h;
+            if (DROPOUT) {
+              const uint32_t bits = kb[cc >> 4] >> ((2 * cc) & 31);
+              sr[cc] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+            } else {
+              sr[cc] = pack_bf16x2(p0, p1);
+            }
           }
         }
       }
@@ -747,20 +772,17 @@ cudaError_t launch_forward_s(const FwdArgs& a, cudaStream_t s) {
                   : launch_fwd_t<128, false, SPARSE, DROPOUT, false, PERSIST>(a, s);
 }
 
-// Dense sequences up to these lengths run persistent CTAs: with few key
-// tiles per item the per-item start-up and epilogue are a large share of the
-// work, and overlapping them pays; longer sequences keep one CTA per item,
-// whose leaner code runs the long key loops faster.  Measured on GB300
-// (causal, persistent against one CTA per item): d = 128 +6 % at N = 4096,
-// +1.4 % at 8192, even at 16384, -1 % at 32768; d = 64 -3 % at 8192.  The
-// dropout kernel keeps the shorter limit (its generator state leaves the
-// persistent loop fewer registers).
+// Dense sequences up to this length run persistent CTAs: with few key tiles
+// per item the per-item start-up and epilogue are a large share of the work,
+// and overlapping them pays; longer sequences keep one CTA per item, whose
+// leaner code runs the long key loops faster.  Measured on GB300 (d = 128,
+// causal, one CTA per item against persistent, with the packed softmax
+// arithmetic): 876 / 900 TFLOP/s at N = 2048, 1098 / 1090 at 4096, 1254 /
+// 1210 at 8192.
 constexpr int kPersistMaxN = 2048;
-constexpr int kPersistMaxN128 = 8192;
 
 bool fwd_persist(const FwdArgs& a) {
-  const int max_n = (a.d == 128 && !a.dropout) ? kPersistMaxN128 : kPersistMaxN;
-  return !a.bmask && a.num_sms > 0 && a.N <= max_n;
+  return !a.bmask && a.num_sms > 0 && a.N <= kPersistMaxN;
 }
 
 }  // namespace
