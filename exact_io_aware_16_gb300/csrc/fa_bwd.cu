@@ -1195,16 +1195,12 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Persistent backward CTAs pay off where tiles are short: the per-tile
-// start-up and epilogue, overlapped with the neighbouring tiles' work, are a
-// large share only when a tile has few steps (measured: +15 % at 4 steps,
-// +9 % at 8.5, -3 % at 16, -1 % at 32).  Dense calls whose tiles average
-// fewer than 16 steps run persistent.
-bool bwd_persist(const BwdArgs& a) {
-  const int nt = (a.N + 127) / 128;
-  const double mean_steps = a.causal ? (nt + 1) / 2.0 : nt;
-  return a.num_sms > 0 && mean_steps < 16.0;
-}
+// Persistent backward CTAs: the next tile's first copies and the current
+// tile's epilogue overlap, which pays most where tiles are short.  Measured on
+// GB300 (persistent against one CTA per tile, causal unless noted): +6 % at
+// B4 H16 N4096 d128, +2-3 % at N = 8192 and 16384, +2.5 % at N = 8192 d64,
+// even at 32768 and non-causal 8192.  Dense calls all run persistent.
+bool bwd_persist(const BwdArgs& a) { return a.num_sms > 0; }
 
 template <bool SPARSE, bool DROPOUT, bool PERSIST>
 cudaError_t launch_dkdv_p(const BwdArgs& a, cudaStream_t s) {

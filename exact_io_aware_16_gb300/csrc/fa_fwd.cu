@@ -547,10 +547,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // row sum adds each pair (p0 + p1) into partial sum (c / 2) % 4, x for
         // even c and y for odd c.  Two pairs at a time, with packed fma / add
         // (each lane rounded as the scalar op, so the sums are the same bit
-        // for bit), except in the dropout kernels and the persistent causal
-        // d = 128 kernel, whose generator or item state leaves no registers
-        // for them (they spilled; the latter ran 8 % slower at N = 2048).
-        constexpr bool kPairs = !DROPOUT && !(PERSIST && CAUSAL && D == 128);
+        // for bit), except in the persistent causal d = 128 kernel, whose item
+        // state leaves no registers for them (it spilled and ran 8 % slower at
+        // N = 2048; the dropout kernels spill a little too but gain 2.5 %).
+        constexpr bool kPairs = !(PERSIST && CAUSAL && D == 128);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           float p[4];
