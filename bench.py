@@ -174,45 +174,72 @@ def barrier(world):
 ORACLE_FULL_HEAD_MAX_N = 8192  # above this one head's full fp64 step takes too long
 
 
-def oracle_sample(w, causal, q, k, v, dO, bh_index=0):
+def oracle_sample(w, causal, q, k, v, dO, bh_index=0, n_rows=None):
     """Time the fp64 oracle (as it stands) on a bounded sample of the
-    workload.  Up to N = 8192: the full forward and backward of one (batch,
-    head) pair.  Beyond: 256 seeded query rows of one pair, forward and the
-    row pass of the backward (dq, m, l, D), whose cost per row is what a
-    full run repeats N times per head.  Returns (seconds, flops of what was
-    computed, cores, description, extrapolated seconds of the full problem
-    at the sampled rate or None)."""
+    workload.  n_rows None and N <= 8192: the full forward and backward of
+    one (batch, head) pair.  Otherwise n_rows (default 256) seeded query rows
+    of one pair, forward and the row pass of the backward (dq, m, l, D),
+    whose cost per row is what a full run repeats N times per head.  Returns
+    (seconds, flops of what was computed, cores, description, extrapolated
+    seconds of the full problem at the sampled rate or None)."""
     import oracle
 
     b, h = divmod(bh_index % (w.B * w.H), w.H)
     qs, ks, vs, ds = (t[b:b + 1, h:h + 1] for t in (q, k, v, dO))
     cores = oracle.default_threads()
-    if w.N <= ORACLE_FULL_HEAD_MAX_N:
+    if n_rows is None and w.N <= ORACLE_FULL_HEAD_MAX_N:
         t0 = time.perf_counter()
         oracle.forward(qs, ks, vs, w.scale, causal, nthreads=cores)
         oracle.backward(qs, ks, vs, ds, w.scale, causal, nthreads=cores)
         dt = time.perf_counter() - t0
         base = w.N * w.N * w.d * (0.5 if causal else 1.0)
-        desc = (f"full fp64 forward+backward of 1 of the {w.B * w.H} (batch, head) pairs "
-                f"({dt:.1f} s; flops counted as 14 N^2 d{' x 1/2 causal' if causal else ''} "
-                f"for what the oracle computes)")
+        desc = (f"full fp64 forward+backward of one (batch, head) pair of {w.B * w.H} "
+                f"(flops counted as 14 N^2 d{' x 1/2 causal' if causal else ''} for what the "
+                f"oracle computes)")
         return dt, 14.0 * base, cores, desc, None
-    rows = sample_indices(w.N, 256, seed=1 + bh_index, must=(0, w.N - 1))
+    n_rows = min(w.N, 256 if n_rows is None else max(1, int(n_rows)))
+    rows = sample_indices(w.N, n_rows, seed=1 + bh_index, must=(0, w.N - 1))
     visible = sum((i + 1) if causal else w.N for i in rows)
     t0 = time.perf_counter()
     oracle.forward(qs, ks, vs, w.scale, causal, rows=rows, nthreads=cores)
     oracle.backward_rows(qs, ks, vs, ds, w.scale, causal, rows=rows, nthreads=cores)
     dt = time.perf_counter() - t0
     fl = 12.0 * visible * w.d  # forward 4 n d + row pass 8 n d per row of n visible keys
-    per_row = dt / len(rows)
-    full_rows = w.B * w.H * w.N
-    mean_visible = visible / len(rows)
     full_visible = w.B * w.H * (w.N * (w.N + 1) / 2 if causal else w.N * w.N)
     extrap = dt * full_visible / visible * (14.0 / 12.0)
-    desc = (f"256 seeded query rows of 1 of the {w.B * w.H} (batch, head) pairs, fp64 forward "
-            f"+ backward row pass ({dt:.1f} s, {per_row * 1e3:.1f} ms per row of "
-            f"{mean_visible:.0f} visible keys on average; {full_rows} rows in the problem)")
+    desc = (f"{len(rows)} seeded query rows of one (batch, head) pair of {w.B * w.H}, fp64 "
+            f"forward + backward row pass ({visible / len(rows):.0f} visible keys per row on "
+            f"average; {w.B * w.H * w.N} rows in the problem)")
     return dt, fl, cores, desc, extrap
+
+
+ORACLE_BASELINE_SECONDS = 10.0  # the CPU baseline samples at least this much oracle work
+ORACLE_BASELINE_MAX_SECONDS = 30.0
+REFERENCE_RUN_SECONDS = 120.0  # the reference arm's warm-up + timed steps together
+
+
+def oracle_baseline(w, causal, q, k, v, dO):
+    """The oracle on successive (batch, head) pairs (or row samples of them)
+    until at least ORACLE_BASELINE_SECONDS of work, never starting a sample
+    that would pass ORACLE_BASELINE_MAX_SECONDS.  Returns (seconds, flops,
+    cores, description, extrapolated full-problem seconds or None)."""
+    tot_t = tot_f = 0.0
+    n = 0
+    cores, desc, extrap, last = 1, "", None, 0.0
+    while n < w.B * w.H and tot_t < ORACLE_BASELINE_SECONDS:
+        if n > 0 and tot_t + last > ORACLE_BASELINE_MAX_SECONDS:
+            break
+        dt, fl, cores, desc, ex = oracle_sample(w, causal, q, k, v, dO, n)
+        tot_t += dt
+        tot_f += fl
+        last = dt
+        n += 1
+        if ex is not None:
+            extrap = ex if extrap is None else extrap
+    desc = f"{n} sample(s), {tot_t:.1f} s in all; each: {desc}"
+    if extrap is not None:
+        extrap = tot_t / tot_f * (14.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0))
+    return tot_t, tot_f, cores, desc, extrap
 
 
 def run_reference(args, world, rank):
@@ -221,11 +248,19 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     q, k, v, dO = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    # every step is a row sample of one (batch, head) pair, sized from a first
+    # 64-row probe so that warm-up and timed steps together take about
+    # REFERENCE_RUN_SECONDS
+    dt0, _, _, _, _ = oracle_sample(w, causal, q, k, v, dO, 0, n_rows=64)
+    per_row = dt0 / min(64, w.N)
+    per_step = REFERENCE_RUN_SECONDS / max(args.steps + args.warmup, 1)
+    n_rows = int(max(16, min(w.N, per_step / max(per_row, 1e-9))))
     for s in range(args.warmup):
-        oracle_sample(w, causal, q, k, v, dO, s)
+        oracle_sample(w, causal, q, k, v, dO, s, n_rows=n_rows)
     tot_t, tot_f, cores, desc = 0.0, 0.0, 1, ""
     for s in range(args.steps):
-        dt, fl, cores, desc, _ = oracle_sample(w, causal, q, k, v, dO, args.warmup + s)
+        dt, fl, cores, desc, _ = oracle_sample(w, causal, q, k, v, dO, args.warmup + s,
+                                               n_rows=n_rows)
         tot_t += dt
         tot_f += fl
     value = tot_f / tot_t / 1e12
@@ -461,7 +496,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, fl, cores, desc, extrap = oracle_sample(w, causal, q_h, k_h, v_h, dO_h, 0)
+        dt, fl, cores, desc, extrap = oracle_baseline(w, causal, q_h, k_h, v_h, dO_h)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": desc}
         if extrap is not None:
