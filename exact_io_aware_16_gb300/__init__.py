@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     fa_forward_fp8,
     fa_forward_tile_count,
     fa_get_device_error,
+    fa_selftest_wait_timeout,
     fa_status_string,
     library,
     library_path,
@@ -35,5 +36,5 @@ __all__ = [
     "fa_forward_dropout", "fa_backward_dropout", "fa_forward_fp8", "fa_backward_preprocess", "fa_backward_dkdv",
     "fa_backward_dq", "fa_backward_noalloc",
     "fa_backward_workspace_size", "fa_forward_tile_count", "fa_get_device_error",
-    "fa_status_string", "library", "library_path",
+    "fa_selftest_wait_timeout", "fa_status_string", "library", "library_path",
 ]

@@ -89,6 +89,8 @@ def library():
         lib.fa_backward_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_backward_dkdv.restype = i
         lib.fa_backward_dq.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_selftest_wait_timeout.argtypes = [vp]
+        lib.fa_selftest_wait_timeout.restype = i
         lib.fa_backward_dq.restype = i
         lib.fa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.fa_get_device_error.restype = i
@@ -483,6 +485,15 @@ def fa_backward_dq(q, k, v, dO, lse, D, causal: bool = False, scale: float | Non
     if st != FA_OK:
         raise FaError(st, "fa_backward_dq")
     return dq
+
+
+def fa_selftest_wait_timeout(stream=None):
+    """Launch the library's failure-reporting self-test: a wait that can never
+    complete gives up after its limit; fa_get_device_error then reports it."""
+    dev = torch.cuda.current_device()
+    st = library().fa_selftest_wait_timeout(ctypes.c_void_p(_stream_handle(stream, dev)))
+    if st != FA_OK:
+        raise FaError(st, "fa_selftest_wait_timeout")
 
 
 def fa_get_device_error(stream=None):

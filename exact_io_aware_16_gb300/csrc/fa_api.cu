@@ -465,16 +465,24 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_selftest_wait_timeout(void* stream) {
+  const int st = check_arch();
+  if (st != FA_OK) return st;
+  return fa::launch_selftest_wait(static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                    : FA_ERR_CUDA;
+}
+
 int fa_get_device_error(void* stream, uint32_t* detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t w_fwd = 0, w_bwd = 0, w_dtc = 0;
+  uint32_t w_fwd = 0, w_bwd = 0, w_dtc = 0, w_st = 0;
   if (fa::fwd_read_clear_error(&w_fwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::bwd_read_clear_error(&w_bwd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::dtc_read_clear_error(&w_dtc, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::st_read_clear_error(&w_st, s) != cudaSuccess) return FA_ERR_CUDA;
   // a launch that gave up may have left its work-item counters dirty
   if (w_fwd && fa::fwd_reset_sched(s) != cudaSuccess) return FA_ERR_CUDA;
   if (w_bwd && fa::bwd_reset_sched(s) != cudaSuccess) return FA_ERR_CUDA;
-  const uint32_t w = w_fwd ? w_fwd : (w_bwd ? w_bwd : w_dtc);
+  const uint32_t w = w_fwd ? w_fwd : (w_bwd ? w_bwd : (w_dtc ? w_dtc : w_st));
   if (detail) *detail = w;
   return w ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }

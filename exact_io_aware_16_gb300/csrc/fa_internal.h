@@ -118,6 +118,12 @@ cudaError_t bwd_reset_sched(cudaStream_t s);
 cudaError_t bwd_read_clear_error(uint32_t* out, cudaStream_t s);
 cudaError_t dtc_read_clear_error(uint32_t* out, cudaStream_t s);
 
+// Self-test of failure reporting: one CTA whose barrier wait runs out (its
+// code, kSelftestWaitCode, lands in the self-test error word).
+constexpr uint32_t kSelftestWaitCode = 0x7e0;
+cudaError_t launch_selftest_wait(cudaStream_t s);
+cudaError_t st_read_clear_error(uint32_t* out, cudaStream_t s);
+
 // Tile counts (host-side mirror of the kernels' loop bounds).
 inline int num_tiles(int N, int tile) { return (N + tile - 1) / tile; }
 

@@ -288,6 +288,18 @@ int fa_host_plan_destroy(fa_host_plan* plan);
  */
 int fa_get_device_error(void* stream, uint32_t* detail);
 
+/*
+ * Self-test of the failure reporting above, without any fault: launches on
+ * `stream` one CTA of 32 threads that waits on a barrier nothing ever arrives
+ * on.  The wait is the same bounded wait every kernel of the library uses; it
+ * gives up after its limit (2 s), records the code 0x7e0 and the kernel
+ * returns normally, so the next fa_get_device_error returns
+ * FA_ERR_DEVICE_TIMEOUT with *detail = 0x800007e0 (timeout flag | code) and
+ * clears it; the context stays usable.  FA_ERR_ARCH off sm_103; FA_ERR_CUDA if
+ * the launch fails.
+ */
+int fa_selftest_wait_timeout(void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(int status);
 

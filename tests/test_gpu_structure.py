@@ -57,6 +57,28 @@ def test_outputs_stay_in_bounds(fa, N, d, causal):
         assert intact(b), f"{name}: write outside the tensor"
 
 
+def test_wait_timeout_is_reported_then_cleared(fa):
+    """A kernel waiting on a barrier nothing arrives on gives up after the
+    bounded wait's limit (2 s) instead of hanging; the error comes back once
+    through fa_get_device_error and the context keeps working."""
+    import time
+
+    assert fa.fa_get_device_error()[0] == 0
+    t0 = time.time()
+    fa.fa_selftest_wait_timeout()
+    st, detail = fa.fa_get_device_error()
+    waited = time.time() - t0
+    assert st == -8 and detail == 0x800007E0, (st, hex(detail))
+    assert 1.0 < waited < 60.0
+    assert fa.fa_get_device_error() == (0, 0)
+    dev = torch.device("cuda")
+    q, k, v, dO = (t.to(dev) for t in make_inputs(1, 2, 300, 64, seed=4))
+    o, lse = fa.fa_forward(q, k, v, causal=True)
+    fa.fa_backward(q, k, v, o, dO, lse, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error()[0] == 0
+
+
 def test_deterministic(fa):
     dev = torch.device("cuda")
     q, k, v, dO = (t.to(dev) for t in make_inputs(2, 4, 1000, 128, seed=9))
