@@ -84,19 +84,94 @@ def alg_bytes(w):
     return 4 * t + r, 8 * t + 2 * r + r  # fwd; bwd incl. D write + read
 
 
+NVML_REASONS = {  # clocks-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlClocks:
+    """Read-only NVML queries (ctypes on the driver's libnvidia-ml): SM clock,
+    its maximum, power draw and the active clocks-event reasons of one GPU."""
+
+    def __init__(self, device_index: int):
+        import ctypes
+
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(device_index)
+        uuid = getattr(props, "uuid", None)
+        ok = False
+        if uuid is not None:
+            ok = lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(self.h)) == 0
+        if not ok:
+            cnt = ctypes.c_uint()
+            if lib.nvmlDeviceGetCount_v2(ctypes.byref(cnt)) != 0 or cnt.value != 1:
+                raise RuntimeError("cannot match the CUDA device to an NVML device")
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        c = self.c
+        clk, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reason_fn(self.h, c.byref(rs))
+        return float(clk.value), mw.value / 1000.0, int(rs.value)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    """SM clock and throttle-reason samples during a timed region.
+
+    NVML is polled every 2 ms from a thread (so that even a 40 ms region gives
+    some twenty samples); where NVML cannot be loaded, nvidia-smi samples every
+    200 ms instead.  mark_load() / mark_done() bracket the timed region on the
+    host: samples taken in between are the ones under load."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_S = 0.002
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.nvml = None
+        self.thread = None
+        self.samples = []
+        self.t_load = self.t_done = None
 
     def start(self):
+        import threading
+
+        try:
+            self.nvml = NvmlClocks(self.dev)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop_flag = threading.Event()
+
+            def run():
+                while not self.stop_flag.is_set():
+                    s = self.nvml.sample()
+                    if s is not None:
+                        self.samples.append((time.perf_counter(),) + s)
+                    time.sleep(self.INTERVAL_S)
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            return
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -108,7 +183,17 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def mark_load(self):
+        self.t_load = time.perf_counter()
+
+    def mark_done(self):
+        self.t_done = time.perf_counter()
+
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            return self._summary_nvml()
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -132,7 +217,24 @@ class ClockSampler:
                           if r[5 + i].lower() in ("active", "1")})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "samples_under_load": None,
+                "source": "nvidia-smi, 200 ms"}
+
+    def _summary_nvml(self):
+        if not self.samples:
+            return None
+        t0 = self.t_load if self.t_load is not None else -math.inf
+        t1 = self.t_done if self.t_done is not None else math.inf
+        load = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
+        reasons = sorted({name for s in load for bit, name in NVML_REASONS.items()
+                          if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in load),
+                "sm_max_mhz": self.nvml.max_mhz,
+                "sm_mhz_min": min(s[1] for s in load),
+                "power_w_max": max(s[2] for s in load),
+                "reasons": reasons, "samples": len(self.samples),
+                "samples_under_load": len([s for s in self.samples if t0 <= s[0] <= t1]),
+                "source": "NVML every 2 ms (read-only queries)"}
 
 
 def dist_setup(args):
@@ -317,6 +419,169 @@ def workload_config(w, causal):
                   f"{5 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB per step > 129 MB)"}
 
 
+KERNELS = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
+
+# MUFU (special-function unit) rate of ex2: 16 results per clock per SM, the
+# throughput table of the CUDA C++ programming guide for compute capability
+# 10.x; the peak is that x SMs x the SM clock (derived, not measured).
+MUFU_EX2_PER_CLK_PER_SM = 16
+
+
+def kernel_work(w, causal):
+    """Per launch of each step kernel: `flops` = the method's matmul work
+    counted once (forward S and P V; backward S recompute, dP, dV and dK in
+    the dK/dV kernel and dQ = dS K alone in the dQ kernel, so the two add up
+    to the step's 10 N^2 d), `exec_flops` = the matmul work the kernel
+    executes (the dQ kernel recomputes S and dP and forms B = P K for the
+    exact D), `exp2` = exponentials of visible score elements, `bytes` = the
+    algorithmic HBM bytes (every tensor once)."""
+    f = 0.5 if causal else 1.0
+    base = w.B * w.H * w.N * w.N * w.d * f
+    e = w.B * w.H * w.N * w.N * f
+    t = w.B * w.H * w.N * w.d * 2  # one bf16 [B,H,N,d] tensor
+    r = w.B * w.H * w.N * 4  # one fp32 [B,H,N] vector
+    return {
+        "fwd": {"flops": 4 * base, "exec_flops": 4 * base, "exp2": e, "bytes": 4 * t + r},
+        "bwd_pre": {"flops": 0.0, "exec_flops": 0.0, "exp2": 0.0, "bytes": 2 * t + r},
+        # reads q, k, v, dO, lse, D~; writes dq and the exact D
+        "bwd_dq": {"flops": 2 * base, "exec_flops": 8 * base, "exp2": e, "bytes": 5 * t + 3 * r},
+        # reads q, k, v, dO, lse, D; writes dk, dv
+        "bwd_dkdv": {"flops": 8 * base, "exec_flops": 8 * base, "exp2": e,
+                     "bytes": 6 * t + 2 * r},
+    }
+
+
+def make_step(fa, w, causal, dev, stream, backward=True, inputs=None):
+    """Device tensors of one workload and a step(ev) that launches its kernels
+    (forward, D pre-pass, dQ, dK/dV) and records ev[i + 1] after kernel i."""
+    q_h, k_h, v_h, dO_h = inputs if inputs is not None else \
+        make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_dO=backward)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    dO = dO_h.to(dev) if backward else None
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    D = torch.empty_like(lse)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3)) if backward else (None,) * 3
+    names = KERNELS if backward else KERNELS[:1]
+
+    def step(ev=None):
+        fa.fa_forward(q, k, v, causal=causal, scale=w.scale, o=o, lse=lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if not backward:
+            return
+        fa.fa_backward_preprocess(o, dO, D, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, scale=w.scale, dq=dq,
+                          stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, scale=w.scale, dk=dk, dv=dv,
+                            stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    return step, names
+
+
+def time_kernels(fa, step, names, steps, warmup, dev, stream, flush=None):
+    """Per-kernel CUDA-event times (ms, summed over `steps`) of step(), after
+    `warmup` untimed steps; with `flush` (a buffer larger than L2) the buffer
+    is rewritten before every step, outside the timed events."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(steps)]
+    for s_ in range(steps):
+        if flush is not None:
+            flush.fill_(s_ & 0xff)
+        evs[s_][0].record(stream)
+        step(evs[s_])
+    torch.cuda.synchronize(dev)
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    return {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(names)}
+
+
+def kernel_table(w, causal, per_kernel_ms, steps, peak, hbm_gbs, mufu_peak):
+    """Per-kernel rates: algorithmic and executed TFLOP/s against the bf16
+    peak, exp2/s against the MUFU peak, algorithmic HBM GB/s, time per launch."""
+    work = kernel_work(w, causal)
+    total = max(sum(per_kernel_ms.values()), 1e-9)
+    out = {}
+    for n, tot in per_kernel_ms.items():
+        ms = tot / steps
+        sec = ms * 1e-3
+        k = {"ms_per_launch": ms, "us_per_launch": ms * 1e3, "share": tot / total}
+        wk = work[n]
+        if wk["flops"]:
+            k["alg_tflops"] = wk["flops"] / sec / 1e12
+            k["frac_of_peak"] = k["alg_tflops"] / peak
+            k["exec_tflops"] = wk["exec_flops"] / sec / 1e12
+        if wk["exp2"]:
+            k["exp2_per_s"] = wk["exp2"] / sec
+            k["exp2_frac_of_mufu"] = k["exp2_per_s"] / mufu_peak
+        k["hbm_gbs"] = wk["bytes"] / sec / 1e9
+        k["hbm_frac"] = k["hbm_gbs"] / hbm_gbs
+        out[n] = k
+    return out
+
+
+def secondary_record(fa, name, dev, stream, steps, peaks, mufu_peak):
+    """Forward and backward TFLOP/s of another workload, timed in this run on
+    resident inputs (its own warm-up; inputs larger than L2)."""
+    w = {**WORKLOADS, **SCALING_WORKLOADS}[name]
+    causal = w.causal[0]
+    step, names = make_step(fa, w, causal, dev, stream)
+    per = time_kernels(fa, step, names, steps, 3, dev, stream)
+    f_fwd, f_bwd = flops(w, causal)
+    fwd_ms = per["fwd"] / steps
+    bwd_ms = sum(per[n] for n in names[1:]) / steps
+    peak = peaks["bf16_tflops"]
+    del step
+    torch.cuda.empty_cache()
+    return {"workload": name, "causal": causal, "steps": steps,
+            "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+            "fwd_frac_of_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
+            "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,
+            "step_tflops": (f_fwd + f_bwd) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+            "ms_per_step": fwd_ms + bwd_ms, "peak_tflops": peak,
+            "kernels": kernel_table(w, causal, per, steps, peak, peaks["hbm_gbs"], mufu_peak),
+            "l2": "inputs larger than L2"}
+
+
+def short_record(fa, name, dev, stream, steps, peaks, mufu_peak):
+    """The short-sequence workloads, where tiles are few and launches short:
+    per-kernel time per launch and algorithmic HBM GB/s as a share of the
+    measured copy bandwidth, L2 flushed (256 MB rewritten) before every step."""
+    w = WORKLOADS[name]
+    causal = w.causal[0]
+    step, names = make_step(fa, w, causal, dev, stream, backward=w.backward)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    per = time_kernels(fa, step, names, steps, 3, dev, stream, flush=flush)
+    # host time to enqueue one step (the C ABI calls and their argument checks)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(8):
+        step()
+    enq_us = (time.perf_counter() - t0) * 1e6 / 8
+    torch.cuda.synchronize(dev)
+    del step, flush
+    torch.cuda.empty_cache()
+    f_fwd, f_bwd = flops(w, causal)
+    ms = sum(per.values()) / steps
+    return {"workload": name, "causal": causal, "steps": steps,
+            "l2": "flushed before every step (256 MB buffer rewritten)",
+            "us_per_step": ms * 1e3, "host_enqueue_us_per_step": enq_us,
+            "step_tflops": (f_fwd + (f_bwd if w.backward else 0.0)) / (ms * 1e-3) / 1e12,
+            "kernels": kernel_table(w, causal, per, steps, peaks["bf16_tflops"],
+                                    peaks["hbm_gbs"], mufu_peak)}
+
+
 def run_ours(args, world, rank, local):
     import exact_io_aware_16_gb300 as fa
     from exact_io_aware_16_gb300 import build as fabuild
@@ -329,36 +594,17 @@ def run_ours(args, world, rank, local):
     w = {**WORKLOADS, **SCALING_WORKLOADS}[args.workload]
     causal = w.causal[0] if args.causal is None else bool(args.causal)
     scale = w.scale
-    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
-    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    D = torch.empty_like(lse)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    inputs = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    q_h, k_h, v_h, dO_h = inputs
     stream = torch.cuda.current_stream(dev)
     if args.fp8:
-        del q, k, v, dO, o, lse, D, dq, dk, dv
         return run_fp8(args, world, rank, local, fa, w, causal, stream, dev)
-    if args.block_mask or args.dropout:
-        return run_variant(args, world, rank, local, fa, w, causal, (q, k, v, dO), stream, dev)
-    if args.decode:
-        return run_decode(args, world, rank, local, fa, w, (q, k, v), stream, dev)
-    names = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
-
-    def step(ev=None):
-        fa.fa_forward(q, k, v, causal=causal, scale=scale, o=o, lse=lse, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        fa.fa_backward_preprocess(o, dO, D, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        fa.fa_backward_dq(q, k, v, dO, lse, D, causal=causal, scale=scale, dq=dq, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-        fa.fa_backward_dkdv(q, k, v, dO, lse, D, causal=causal, scale=scale, dk=dk, dv=dv,
-                            stream=stream)
-        if ev is not None:
-            ev[4].record(stream)
+    if args.block_mask or args.dropout or args.decode:
+        tensors = tuple(t.to(dev) for t in inputs)
+        if args.decode:
+            return run_decode(args, world, rank, local, fa, w, tensors[:3], stream, dev)
+        return run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev)
+    step, names = make_step(fa, w, causal, dev, stream, inputs=inputs)
 
     for _ in range(args.warmup):
         step()
@@ -374,6 +620,7 @@ def run_ours(args, world, rank, local):
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    clocks.mark_load()
     t_start.record(stream)
     h0 = time.perf_counter()
     n_enq = min(args.steps, 8)  # before the launch queue can fill and block the host
@@ -385,6 +632,7 @@ def run_ours(args, world, rank, local):
             enqueue_us = (time.perf_counter() - h0) * 1e6 / n_enq  # host side, per step
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_done()
     barrier(world)
     clk = clocks.stop()
     st, detail = fa.fa_get_device_error(stream)
@@ -404,62 +652,66 @@ def run_ours(args, world, rank, local):
     long_region = total_ms > 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     peak_kind = "sustained" if long_region else "burst"
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = (clk or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    mufu_peak = MUFU_EX2_PER_CLK_PER_SM * num_sms * sm_mhz * 1e6
     fwd_ms = per_kernel["fwd"] / args.steps
     bwd_ms = (per_kernel["bwd_pre"] + per_kernel["bwd_dkdv"] + per_kernel["bwd_dq"]) / args.steps
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
-    # diagnostics: HBM share of the algorithmic bytes (the measure that matters
-    # for the short, low-intensity workloads), exp2 rate, host enqueue time
+    kernels = kernel_table(w, causal, per_kernel, args.steps, peak, peaks["hbm_gbs"], mufu_peak)
     fwd_bytes, bwd_bytes = alg_bytes(w)
     diag = {
         "fwd_hbm_gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9,
         "fwd_hbm_frac": fwd_bytes / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "bwd_hbm_gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
         "bwd_hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-        "fwd_exp2_per_s": w.B * w.H * w.N * w.N * (0.5 if causal else 1.0) / (fwd_ms * 1e-3),
+        "fwd_exp2_per_s": kernels["fwd"]["exp2_per_s"],
+        "mufu_peak_exp2_per_s": mufu_peak,
+        "mufu_peak_derivation": (f"{MUFU_EX2_PER_CLK_PER_SM} ex2 per clock per SM (CUDA "
+                                 f"programming guide, compute capability 10.x) x {num_sms} SMs "
+                                 f"x {sm_mhz:.0f} MHz (median SM clock in the timed region)"),
         "host_enqueue_us_per_step": enqueue_us,
         "device_us_per_step": ms_per_step * 1e3,
     }
 
-    # dominant kernel and its roofline (algorithmic work of that kernel alone)
-    base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
-    # per-kernel algorithmic FLOPs: the matmuls that kernel's own outputs require
-    # (dQ needs S, dP and dS K; dK/dV need S, dP, P^T dO and dS^T Q), so the
-    # recomputed S and dP count in both backward kernels
-    kflops = {"fwd": 4 * base, "bwd_dkdv": 8 * base, "bwd_dq": 6 * base, "bwd_pre": 0.0}
-    tbytes = w.B * w.H * w.N * w.d * 2
-    kbytes = {"bwd_pre": 2 * tbytes + w.B * w.H * w.N * 4}
+    # dominant kernel and its roofline: the method's work of that kernel alone,
+    # counted once (kernel_work)
     dom = max(names, key=lambda n: per_kernel[n])
     dom_ms = per_kernel[dom] / args.steps
+    trace = captured_traffic(dom, w.name) if causal == w.causal[0] else None
     if dom == "bwd_pre":
-        ach = kbytes[dom] / (dom_ms * 1e-3) / 1e9
+        ach = kernels[dom]["hbm_gbs"]
         roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
-                "traffic": captured_traffic(dom, w.name) if causal == w.causal[0] else None}
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": trace}
     else:
-        ach = kflops[dom] / (dom_ms * 1e-3) / 1e12
+        ach = kernels[dom]["alg_tflops"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": captured_traffic(dom, w.name) if causal == w.causal[0] else None,
-                "peak_kind": f"{peak_kind} bf16 ({peak_src})"}
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": trace,
+                "peak_kind": f"{peak_kind} bf16 ({peak_src})",
+                "work": "the method's matmuls of this kernel counted once (dK/dV 8 N^2 d, "
+                        "dQ 2 N^2 d, forward 4 N^2 d per head, x1/2 causal)"}
     roof["ms_per_launch"] = dom_ms
 
-    kernels = {}
-    for n in names:
-        ms = per_kernel[n] / args.steps
-        kernels[n] = {"ms_per_launch": ms, "share": per_kernel[n] / max(sum(per_kernel.values()),
-                                                                         1e-9)}
-        if kflops.get(n):
-            kernels[n]["alg_tflops"] = kflops[n] / (ms * 1e-3) / 1e12
+    # headline-adjacent workloads, timed in this run (rank 0, one GPU)
+    secondary = short = None
+    if rank == 0 and world == 1 and not args.no_secondary:
+        del step
+        torch.cuda.empty_cache()
+        sec_steps = max(3, min(args.steps, 20))
+        secondary = secondary_record(fa, "causal_b1h32n32768d128_qk2", dev, stream, sec_steps,
+                                     peaks, mufu_peak)
+        short = [short_record(fa, n, dev, stream, 50, peaks, mufu_peak)
+                 for n in ("fwd_b1h2n256d64", "short_b64h12n512d64")]
 
     # end to end through the C ABI's host-buffer runtime (fa_host_step): every
     # step copies its inputs in from pinned host memory and its outputs
     # (o, lse, dq, dk, dv) back; copies of neighbouring steps overlap the
     # kernels of the current one; host wall clock from the first call to the
-    # end of fa_host_wait
+    # end of fa_host_wait, over at least E2E_MIN_STEPS steps and E2E_MIN_SECONDS
     e2e = None
     if not args.no_e2e:
-        del o, lse, D, dq, dk, dv  # the plan holds its own device buffers
+        step = None
         torch.cuda.empty_cache()
         sets = []
         for i in range(2):  # two host buffer sets, alternated between steps
@@ -473,10 +725,13 @@ def run_ours(args, world, rank, local):
             (qh, kh, vh, dOh), (oh, dqh, dkh, dvh, lseh) = sets[i % 2]
             plan.step(qh, kh, vh, dOh, oh, lseh, dqh, dkh, dvh)
 
-        for i in range(max(2, args.warmup // 2)):
+        n_warm = max(4, args.warmup)
+        t0 = time.perf_counter()
+        for i in range(n_warm):
             e2e_step(i)
         plan.wait()
-        n_e2e = max(4, args.steps // 4)
+        est = (time.perf_counter() - t0) / n_warm
+        n_e2e = int(min(E2E_MAX_STEPS, max(E2E_MIN_STEPS, math.ceil(E2E_MIN_SECONDS / est))))
         torch.cuda.synchronize(dev)
         barrier(world)
         t0 = time.perf_counter()
@@ -490,7 +745,7 @@ def run_ours(args, world, rank, local):
         e2e = {"value": aggregate_rate(f_fwd + f_bwd, world, e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "steps": n_e2e,
+               "steps": n_e2e, "seconds": n_e2e * e_ms * 1e-3,
                "how": "fa_host_step (C ABI, pinned host buffers, two-slot copy/compute "
                       "pipeline), host wall clock"}
 
@@ -513,9 +768,15 @@ def run_ours(args, world, rank, local):
             "peak_tflops": peak, "peak_source": f"{peak_kind} bf16, {peak_src}",
             "kernels": kernels, "roofline": roof, "diagnostics": diag, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk,
+            "secondary": secondary, "short_sequence": short,
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+E2E_MIN_STEPS = 100
+E2E_MIN_SECONDS = 1.0
+E2E_MAX_STEPS = 4000
 
 
 def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
@@ -751,6 +1012,8 @@ def main():
                     help="time the decode step with this many query rows (<= 16)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the 32K and short-sequence records timed after the main one")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -116,15 +116,30 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on_device(t) -> bool:
+    return bool(t.is_cuda)
+
+
 def _check(t, name, dtype, shape=None):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
+    if not _on_device(t):
         raise TypeError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_grads(dq, dk, dv, shape):
+    for t, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, nm, torch.bfloat16, shape)
+
+
+def _check_workspace(ws):
+    if not isinstance(ws, torch.Tensor) or not _on_device(ws) or not ws.is_contiguous() \
+            or ws.dtype != torch.uint8:
+        raise TypeError("workspace must be a contiguous uint8 CUDA tensor")
 
 
 def fa_forward_tile_count(N: int, causal: bool) -> int:
@@ -156,7 +171,7 @@ def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, o=None
 def _mask_args(mask, B, H, N):
     """(pointer, head stride) of a uint8 CUDA block mask [nt,nt] or [B*H,nt,nt]."""
     nt = -(-N // 128)
-    if mask.dtype != torch.uint8 or not mask.is_cuda or not mask.is_contiguous():
+    if mask.dtype != torch.uint8 or not _on_device(mask) or not mask.is_contiguous():
         raise TypeError("block mask must be a contiguous uint8 CUDA tensor")
     if tuple(mask.shape) == (nt, nt):
         return ctypes.c_void_p(mask.data_ptr()), 0
@@ -174,6 +189,8 @@ def fa_forward_blocksparse(q, k, v, block_mask, causal: bool = False, scale: flo
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
     mp, ms = _mask_args(block_mask, B, H, N)
     st = library().fa_forward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
                                           d, float(scale), int(bool(causal)), mp, ms,
@@ -195,9 +212,11 @@ def fa_backward_blocksparse(q, k, v, o, dO, lse, block_mask, causal: bool = Fals
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_grads(dq, dk, dv, (B, H, N, d))
     need = fa_backward_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace)
     mp, ms = _mask_args(block_mask, B, H, N)
     st = library().fa_backward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
                                            _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
@@ -246,11 +265,11 @@ def fa_backward_dropout(q, k, v, o, dO, lse, p_drop: float, seed: int, offset: i
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check_grads(dq, dk, dv, (B, H, N, d))
     need = fa_backward_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace)
     mp, ms = (None, 0) if block_mask is None else _mask_args(block_mask, B, H, N)
     st = library().fa_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                                        _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
@@ -414,11 +433,11 @@ def fa_backward(q, k, v, o, dO, lse, causal: bool = False, scale: float | None =
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _check(t, nm, torch.bfloat16, (B, H, N, d))
+    _check_grads(dq, dk, dv, (B, H, N, d))
     need = fa_backward_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace)
     st = library().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                int(bool(causal)), _ptr(workspace), workspace.numel(),
@@ -440,6 +459,7 @@ def fa_backward_noalloc(q, k, v, o, dO, lse, causal: bool = False, scale: float 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_grads(dq, dk, dv, (B, H, N, d))
     st = library().fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                                        _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                        int(bool(causal)),
@@ -460,6 +480,8 @@ def fa_backward_dkdv(q, k, v, dO, lse, D, causal: bool = False, scale: float | N
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check(dk, "dk", torch.bfloat16, (B, H, N, d))
+    _check(dv, "dv", torch.bfloat16, (B, H, N, d))
     st = library().fa_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
                                     _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                     int(bool(causal)),
@@ -479,6 +501,7 @@ def fa_backward_dq(q, k, v, dO, lse, D, causal: bool = False, scale: float | Non
     _check(D, "D", torch.float32, (B, H, N))
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
+    _check(dq, "dq", torch.bfloat16, (B, H, N, d))
     st = library().fa_backward_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
                                   _ptr(dq), B, H, N, d, float(scale), int(bool(causal)),
                                   ctypes.c_void_p(_stream_handle(stream, q.device)))

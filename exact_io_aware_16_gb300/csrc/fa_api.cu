@@ -1,5 +1,6 @@
 // fa_api.cu — the C ABI of libfa: argument validation, TMA tensor-map
 // construction and kernel launches.  No device memory is allocated here.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -32,13 +33,7 @@ EncodeTiledFn get_encode_tiled() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
-  const long long total = static_cast<long long>(B) * H * N * d;
-  if (total >= (1ll << 31)) return FA_ERR_SHAPE;
-  return FA_OK;
-}
+int check_shape(int B, int H, int N, int d) { return fa::check_bhnd(B, H, N, d); }
 
 int check_scale(float scale) {
   if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_SHAPE;
@@ -49,14 +44,14 @@ int check_scale(float scale) {
 int check_arch() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FA_ERR_CUDA;
-  static int cache[64];  // 0 unknown, 1 ok, 2 bad
-  if (dev < 64 && cache[dev] == 1) return FA_OK;
+  static std::atomic<int> cache[64];  // 0 unknown, 1 ok, 2 bad (any thread may fill it)
+  if (dev < 64 && cache[dev].load(std::memory_order_relaxed) == 1) return FA_OK;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
   const bool ok = (major == 10 && minor == 3);
-  if (dev < 64) cache[dev] = ok ? 1 : 2;
+  if (dev < 64) cache[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok ? FA_OK : FA_ERR_ARCH;
 }
 
@@ -99,12 +94,15 @@ int encode_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols) {
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  static int cache[64];
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  static std::atomic<int> cache[64];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
     n = 1;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -405,11 +403,15 @@ int fa_forward_fp8(const void* q8, const void* k8, const void* vt8, float q_desc
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Decode shapes: the cache as for check_bhnd (B*H a TMA coordinate, its key
+// tiles an int32 count), and the (head, key range) CTAs of the split kernel
+// within an int32 grid.
 static int check_decode_shape(int B, int H, int Nq, int Nk, int d) {
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || Nq > fa::kMaxDecodeQueries) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
-  const long long total = static_cast<long long>(B) * H * Nk * d;
-  if (total >= (1ll << 31)) return FA_ERR_SHAPE;
+  if (Nq < 1 || Nq > fa::kMaxDecodeQueries) return FA_ERR_SHAPE;
+  const int st = fa::check_bhnd(B, H, Nk, d);
+  if (st != FA_OK) return st;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH * fa::decode_splits(BH, Nk) > 0x7fffffffll) return FA_ERR_SHAPE;
   return FA_OK;
 }
 

@@ -44,7 +44,6 @@ __device__ unsigned int g_bwd_error;
 // claims a slot, its CTAs take items with atomicAdd on slot[0], the last CTA
 // to finish (slot[1] counts them) zeroes the slot; bwd_reset_sched zeroes all
 // slots after a device error.
-constexpr int kSchedSlots = 1024;
 __device__ unsigned int g_bwd_sched[kSchedSlots][2];
 constexpr int kItemRing = 4;  // claimed items in flight between the roles of a CTA
 
@@ -1128,30 +1127,17 @@ int bwd_group_heads(const BwdArgs& a) {
   return static_cast<int>(g < 1.0 ? 1.0 : (g > a.BH ? a.BH : g));
 }
 
-// A counter slot of g_bwd_sched for the next persistent launch on the
-// current device (slots are handed out in turn).
-cudaError_t claim_sched_slot(unsigned int** out) {
-  static std::mutex mu;
-  static unsigned int* base[64] = {};  // g_bwd_sched's address per device
-  static unsigned int next_slot = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!base[dev]) {
-    void* p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_bwd_sched)) != cudaSuccess) return e;
-    base[dev] = static_cast<unsigned int*>(p);
-  }
-  *out = base[dev] + 2 * (next_slot++ % kSchedSlots);
-  return cudaSuccess;
+// Counter slots of this file's persistent launches (see SchedRing).
+SchedRing g_sched_ring;
+
+cudaError_t claim_slot(cudaStream_t s, unsigned int** out) {
+  return claim_sched_slot(g_sched_ring, reinterpret_cast<const void*>(&g_bwd_sched), s, out);
 }
 
 // Grid of a backward launch: persistent (one CTA per SM, items claimed from
 // a counter slot) or one CTA per item.
 template <bool PERSIST>
-cudaError_t bwd_grid(const BwdArgs& a, unsigned* blocks, unsigned int** sched) {
+cudaError_t bwd_grid(const BwdArgs& a, cudaStream_t s, unsigned* blocks, unsigned int** sched) {
   const long long items = static_cast<long long>((a.N + 127) / 128) * a.BH;
   if (items > 0x7fffffffll) return cudaErrorInvalidValue;
   *sched = nullptr;
@@ -1161,7 +1147,7 @@ cudaError_t bwd_grid(const BwdArgs& a, unsigned* blocks, unsigned int** sched) {
   }
   if (a.num_sms < 1) return cudaErrorInvalidValue;
   *blocks = static_cast<unsigned>(std::min<long long>(items, a.num_sms));
-  return claim_sched_slot(sched);
+  return claim_slot(s, sched);
 }
 
 template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool PERSIST>
@@ -1172,7 +1158,7 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   unsigned blocks = 0;
   unsigned int* sched = nullptr;
-  if ((e = bwd_grid<PERSIST>(a, &blocks, &sched)) != cudaSuccess) return e;
+  if ((e = bwd_grid<PERSIST>(a, s, &blocks, &sched)) != cudaSuccess) return e;
   kern<<<blocks, kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.scale, a.scale_log2, a.bmask, a.mstride,
@@ -1188,7 +1174,7 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   unsigned blocks = 0;
   unsigned int* sched = nullptr;
-  if ((e = bwd_grid<PERSIST>(a, &blocks, &sched)) != cudaSuccess) return e;
+  if ((e = bwd_grid<PERSIST>(a, s, &blocks, &sched)) != cudaSuccess) return e;
   kern<<<blocks, kBwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, *a.tdo, a.lse, a.D, static_cast<__nv_bfloat16*>(a.dq), a.BH, a.N,
       a.scale, a.scale_log2, a.bmask, a.mstride, a.drop, bwd_group_heads(a), sched);

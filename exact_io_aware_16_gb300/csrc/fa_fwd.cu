@@ -61,7 +61,6 @@ __device__ unsigned int g_fwd_error;
 // slot[0], and the last CTA to finish (slot[1] counts them) zeroes the slot
 // again.  fa_fwd_reset_sched zeroes every slot after a device error, since an
 // aborted launch may leave its slot dirty.
-constexpr int kSchedSlots = 1024;
 __device__ unsigned int g_fwd_sched[kSchedSlots][2];
 constexpr int kItemRing = 4;  // claimed items in flight between the roles of a CTA
 
@@ -716,24 +715,11 @@ int group_heads(const FwdArgs& a) {
   return static_cast<int>(g < 1.0 ? 1.0 : (g > a.BH ? a.BH : g));
 }
 
-// A counter slot of g_fwd_sched for the next persistent launch on the
-// current device (slots are handed out in turn).
-cudaError_t claim_sched_slot(unsigned int** out) {
-  static std::mutex mu;
-  static unsigned int* base[64] = {};  // g_fwd_sched's address per device
-  static unsigned int next_slot = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!base[dev]) {
-    void* p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_fwd_sched)) != cudaSuccess) return e;
-    base[dev] = static_cast<unsigned int*>(p);
-  }
-  *out = base[dev] + 2 * (next_slot++ % kSchedSlots);
-  return cudaSuccess;
+// Counter slots of this file's persistent launches (see SchedRing).
+SchedRing g_sched_ring;
+
+cudaError_t claim_slot(cudaStream_t s, unsigned int** out) {
+  return claim_sched_slot(g_sched_ring, reinterpret_cast<const void*>(&g_fwd_sched), s, out);
 }
 
 template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool FP8 = false, bool PERSIST = false>
@@ -755,7 +741,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   unsigned int* sched = nullptr;
   if (kPersist) {
     if (a.num_sms < 1) return cudaErrorInvalidValue;
-    if ((e = claim_sched_slot(&sched)) != cudaSuccess) return e;
+    if ((e = claim_slot(s, &sched)) != cudaSuccess) return e;
   }
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, smem, s>>>(
       *a.tq, *a.tk, *a.tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N, a.scale_log2,

@@ -76,9 +76,8 @@ int fa_host_plan_create(int B, int H, int N, int d, float scale, int causal,
                         fa_host_plan** plan) {
   if (!plan) return FA_ERR_NULL;
   *plan = nullptr;
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
-  if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return FA_ERR_SHAPE;
+  const int shape_st = fa::check_bhnd(B, H, N, d);
+  if (shape_st != FA_OK) return shape_st;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_SHAPE;
   const size_t ws = fa_backward_workspace_size(B, H, N, d);
   if (ws == 0) return FA_ERR_SHAPE;

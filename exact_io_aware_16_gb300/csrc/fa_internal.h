@@ -3,9 +3,11 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/fa.h"
 #include "philox.cuh"
 
 namespace fa {
@@ -124,7 +126,67 @@ constexpr uint32_t kSelftestWaitCode = 0x7e0;
 cudaError_t launch_selftest_wait(cudaStream_t s);
 cudaError_t st_read_clear_error(uint32_t* out, cudaStream_t s);
 
+// Work-item counter slots of a kernel file's persistent launches.  A
+// persistent launch is given one slot ({claimed items, finished CTAs}); its
+// CTAs claim items with atomicAdd on the first word and the launch's last CTA
+// zeroes both words.  Eager launches take slots [0, kEagerSlots) in turn.  A
+// launch made while its stream is being captured into a CUDA graph keeps its
+// slot for every replay, so captured launches take slots from a separate ring
+// [kEagerSlots, kSchedSlots): an eager launch never shares a slot with a graph.
+// (Replays of one graph that run at the same time on different streams share
+// its slots and must not overlap.)
+constexpr int kSchedSlots = 1024;
+constexpr int kEagerSlots = 768;
+
+struct SchedRing {
+  std::mutex mu;
+  unsigned int* base[64] = {};  // the slot array's device address per device
+  unsigned int next_eager = 0;
+  unsigned int next_capture = 0;
+};
+
+// Claims the next slot of `ring` for a launch on stream s of the current
+// device.  `symbol` is the host-side stand-in of the kernel file's
+// __device__ unsigned int[kSchedSlots][2]; its device address is looked up
+// once per device (the first persistent launch on a device should come
+// before any stream capture).
+inline cudaError_t claim_sched_slot(SchedRing& ring, const void* symbol, cudaStream_t s,
+                                    unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(ring.mu);
+  if (!ring.base[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, symbol)) != cudaSuccess) return e;
+    ring.base[dev] = static_cast<unsigned int*>(p);
+  }
+  const unsigned int slot =
+      cap == cudaStreamCaptureStatusActive
+          ? kEagerSlots + ring.next_capture++ % (kSchedSlots - kEagerSlots)
+          : ring.next_eager++ % kEagerSlots;
+  *out = ring.base[dev] + 2 * slot;
+  return cudaSuccess;
+}
+
 // Tile counts (host-side mirror of the kernels' loop bounds).
 inline int num_tiles(int N, int tile) { return (N + tile - 1) / tile; }
+
+// Shape rules shared by every [B][H][N][d] entry point.  Device offsets are
+// 64-bit throughout, so the element count is not limited to 32 bits; what is
+// limited is B*H (the third coordinate of the TMA tensor maps, an int32) and
+// the work items of one launch, B*H*ceil(N/128) (an int32 item index).  Those
+// bound B*H*N*d*4 well below 2^63, so every byte size fits in size_t.
+inline int check_bhnd(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffll) return FA_ERR_SHAPE;
+  if (BH * num_tiles(N, kTileM) > 0x7fffffffll) return FA_ERR_SHAPE;
+  return FA_OK;
+}
 
 }  // namespace fa

@@ -26,7 +26,10 @@
  *    natural-log logsumexp of row i of the SCALED scores scale*q_i.k_j.
  *  - causal != 0 masks key j for query i when j > i (square, top-left
  *    aligned); masked scores are -inf before the softmax.
- *  - d must be 64 or 128; B, H, N >= 1; B*H*N*d < 2^31; scale > 0 and finite.
+ *  - d must be 64 or 128; B, H, N >= 1; scale > 0 and finite.  B*H must be
+ *    below 2^31 (it is a coordinate of the TMA tensor maps) and so must
+ *    B*H*ceil(N/128) (the work items of one launch); FA_ERR_SHAPE otherwise.
+ *    There is no limit on B*H*N*d itself: every device offset is 64-bit.
  *  - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.
  *    The library allocates no device memory in these calls.  In-place use
  *    (an output aliasing an input) is undefined.
@@ -35,6 +38,12 @@
  *    are returned immediately and nothing is launched.  A launch failure
  *    returns FA_ERR_CUDA.  A device-side pipeline timeout is reported later
  *    by fa_get_device_error().
+ *  - A recorded timeout is sticky: until fa_get_device_error() reads and
+ *    clears it, every later launch of this library on the device exits at
+ *    entry without computing anything, while the calls that made those
+ *    launches still return FA_OK.  Outputs written after a timeout are
+ *    therefore stale until the record is cleared: check fa_get_device_error()
+ *    (or fa_host_wait(), which does the same) before trusting results.
  *  - Only sm_103 (GB300) devices are accepted (FA_ERR_ARCH otherwise).
  */
 #ifndef FA_H_
@@ -238,7 +247,8 @@ int fa_forward_fp8(const void* q8, const void* k8, const void* vt8, float q_desc
  * 11:33).  q [B][H][Nq][d], k and v [B][H][Nk][d] bf16; o [B][H][Nq][d] bf16,
  * lse [B][H][Nq] fp32.  Query i sits at cache position Nk - Nq + i: with
  * causal != 0 it sees keys 0 .. Nk - Nq + i, else all Nk keys.  1 <= Nq <= 16,
- * Nk >= 1 (Nk >= Nq when causal), d in {64, 128}.  The key axis is split into
+ * Nk >= 1 (Nk >= Nq when causal), d in {64, 128}; B, H and Nk obey the shape
+ * rules above (with Nk for N).  The key axis is split into
  * ranges processed in parallel, merged by the online-softmax update; the
  * workspace (device memory, 256-byte aligned, contents irrelevant) holds the
  * partial results: fa_decode_workspace_size() bytes.  Errors as fa_forward,
@@ -268,7 +278,10 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
  *    copies that block the calling thread).
  *  - fa_host_wait: blocks until every enqueued step has finished and its
  *    outputs are in host memory; returns the first device error, as
- *    fa_get_device_error does.
+ *    fa_get_device_error does (and clears it).  fa_host_step itself never
+ *    reads the device error record: after a timeout, the steps enqueued
+ *    before the next fa_host_wait produce stale outputs, and only that
+ *    fa_host_wait's FA_ERR_DEVICE_TIMEOUT reports it.
  *  - fa_host_plan_destroy: waits, then frees the plan (NULL is a no-op).
  * Argument errors as for fa_forward; NULL pointers give FA_ERR_NULL.
  */

@@ -60,7 +60,7 @@ def test_forward_validation(lib):
     assert fwd(lib, scale=0.0) == -2
     assert fwd(lib, scale=-1.0) == -2
     assert fwd(lib, scale=float("inf")) == -2
-    assert fwd(lib, B=1 << 15, H=1 << 15, N=4, d=64) == -2  # B*H*N*d >= 2^31
+    assert fwd(lib, B=1 << 16, H=1 << 15, N=4, d=64) == -2  # B*H >= 2^31
     assert fwd(lib, q=FAKE + 8) == -4
     assert fwd(lib, o=FAKE + 2) == -4
     assert fwd(lib, lse=FAKE + 4) == -4
@@ -84,6 +84,29 @@ def test_backward_validation(lib):
     assert bwd(lib, ws_bytes=100) == -6
     assert bwd(lib, ws=FAKE * 16 + 16) == -6  # workspace must be 256-byte aligned
     assert bwd(lib, dk=FAKE + 4) == -4
+
+
+def test_shapes_beyond_2_31_elements(lib):
+    """B*H*N*d is not limited to 32 bits; B*H and the work items of a launch
+    (B*H*ceil(N/128)) are.  Each call below passes the shape check and then
+    fails the alignment check that follows it (FA_ERR_ALIGN), so nothing is
+    launched on any machine."""
+    # 2^36 elements: B*H = 2^20, N = 512, d = 128
+    big = dict(B=1 << 10, H=1 << 10, N=512, d=128)
+    assert fwd(lib, q=FAKE + 8, **big) == -4
+    assert bwd(lib, dq=FAKE + 8, ws_bytes=1 << 40, **big) == -4
+    n = 4 * (1 << 20) * 512
+    assert lib.fa_backward_workspace_size(1 << 10, 1 << 10, 512, 128) == n
+    # largest allowed item count: B*H*ceil(N/128) = 2^31 - 1
+    assert fwd(lib, q=FAKE + 8, B=1, H=(1 << 31) - 1, N=128, d=64) == -4
+    # one more item, or B*H = 2^31, is refused
+    assert fwd(lib, q=FAKE + 8, B=1, H=(1 << 30), N=257, d=64) == -2
+    assert fwd(lib, q=FAKE + 8, B=2, H=1 << 30, N=1, d=64) == -2
+    assert lib.fa_backward_workspace_size(2, 1 << 30, 1, 64) == 0
+    # decode: a 2^33-element cache is accepted by the shape check
+    assert lib.fa_decode(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 64, 4, 1 << 20, 128, 0.125, 0,
+                         FAKE * 16, 1 << 40, None) == -4
+    assert lib.fa_decode_workspace_size(1, 64, 4, 1 << 20, 128) > 0
 
 
 def test_blocksparse_validation(lib):

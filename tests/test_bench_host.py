@@ -82,3 +82,62 @@ def test_reference_arm_fits_its_time_budget(monkeypatch, capsys, steps, warmup):
         assert total == pytest.approx(bench.REFERENCE_RUN_SECONDS, rel=0.02)
     else:
         assert total <= bench.REFERENCE_RUN_SECONDS * 1.5 or rows == 16
+
+
+@pytest.mark.parametrize("name", ["causal_b2h16n8192d128", "b4h16n2048d64",
+                                  "short_b64h12n512d64"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_kernel_work_counts_the_method_once(name, causal):
+    """The backward kernels' method work sums to the step's 10 N^2 d (S
+    recomputed once), the forward's is 4 N^2 d, and the executed work of the
+    dQ kernel is its four products (S, dP, B = P K, dQ)."""
+    w = WORKLOADS[name]
+    kw = bench.kernel_work(w, causal)
+    f_fwd, f_bwd = bench.flops(w, causal)
+    assert kw["fwd"]["flops"] == f_fwd
+    assert kw["bwd_dq"]["flops"] + kw["bwd_dkdv"]["flops"] == f_bwd
+    base = w.B * w.H * w.N * w.N * w.d * (0.5 if causal else 1.0)
+    assert kw["bwd_dq"]["exec_flops"] == 8 * base and kw["bwd_dkdv"]["exec_flops"] == 8 * base
+    t = w.B * w.H * w.N * w.d * 2
+    r = w.B * w.H * w.N * 4
+    fwd_b, bwd_b = bench.alg_bytes(w)
+    assert kw["fwd"]["bytes"] == fwd_b
+    # every backward input once (q, k, v, dO, o, lse, D read; dq, dk, dv, D written)
+    # is read or written by exactly the kernels that need it
+    assert kw["bwd_pre"]["bytes"] == 2 * t + r
+    assert kw["bwd_dq"]["bytes"] == 5 * t + 3 * r
+    assert kw["bwd_dkdv"]["bytes"] == 6 * t + 2 * r
+
+
+def test_kernel_table_rates():
+    w = WORKLOADS["causal_b2h16n8192d128"]
+    per = {"fwd": 4.5, "bwd_pre": 0.25, "bwd_dq": 7.5, "bwd_dkdv": 7.5}  # ms over 10 steps
+    tab = bench.kernel_table(w, True, per, 10, 2000.0, 7000.0, 5e12)
+    kw = bench.kernel_work(w, True)
+    assert tab["bwd_dkdv"]["alg_tflops"] == pytest.approx(kw["bwd_dkdv"]["flops"] / 0.75e-3 / 1e12)
+    assert tab["bwd_dq"]["frac_of_peak"] == pytest.approx(tab["bwd_dq"]["alg_tflops"] / 2000.0)
+    assert tab["bwd_dq"]["exec_tflops"] == pytest.approx(4 * tab["bwd_dq"]["alg_tflops"])
+    assert tab["fwd"]["us_per_launch"] == pytest.approx(450.0)
+    assert "alg_tflops" not in tab["bwd_pre"]
+    assert sum(k["share"] for k in tab.values()) == pytest.approx(1.0)
+    assert tab["fwd"]["exp2_frac_of_mufu"] == pytest.approx(
+        w.B * w.H * w.N * w.N * 0.5 / 0.45e-3 / 5e12)
+
+
+def test_clock_summary_counts_samples_in_the_timed_region():
+    """NVML samples (time, MHz, W, reason bits): only those between
+    mark_load and mark_done count as under load, and reasons are decoded."""
+
+    class FakeNvml:
+        max_mhz = 2070.0
+
+    cs = bench.ClockSampler(0)
+    cs.nvml = FakeNvml()
+    cs.samples = [(0.0, 1000.0, 100.0, 0x1), (1.0, 2070.0, 900.0, 0x4), (1.5, 2040.0, 950.0, 0x0),
+                  (2.0, 2070.0, 1000.0, 0x0), (3.0, 1200.0, 200.0, 0x1)]
+    cs.t_load, cs.t_done = 0.9, 2.1
+    s = cs._summary_nvml()
+    assert s["samples"] == 5 and s["samples_under_load"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_mhz_min"] == 2040.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_max"] == 1000.0

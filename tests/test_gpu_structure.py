@@ -114,7 +114,12 @@ def test_errors_on_device(fa):
 
 def test_memory_linear_in_n(fa):
     """Beyond inputs and outputs, the backward needs only its fp32 [B,H,N]
-    workspace; peak allocation grows linearly with N."""
+    workspace, so device memory grows linearly with N; the library itself
+    allocates nothing.  Measured two ways: PyTorch's allocator statistics
+    (nothing allocated through PyTorch) and the device's free memory from
+    cudaMemGetInfo, which would also show a cudaMalloc made inside libfa.so.
+    Each size runs once untimed first, so that the first launch of each kernel
+    (module loading) is not counted."""
     dev = torch.device("cuda")
     extra = []
     for N in (2048, 4096, 8192):
@@ -124,13 +129,21 @@ def test_memory_linear_in_n(fa):
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
         ws = torch.empty(fa.fa_backward_workspace_size(1, 4, N, 128), dtype=torch.uint8,
                          device=dev)
+
+        def step():
+            fa.fa_forward(q, k, v, causal=True, o=o, lse=lse)
+            fa.fa_backward(q, k, v, o, dO, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        step()
         torch.cuda.synchronize()
         torch.cuda.reset_peak_memory_stats()
         base = torch.cuda.memory_allocated()
-        fa.fa_forward(q, k, v, causal=True, o=o, lse=lse)
-        fa.fa_backward(q, k, v, o, dO, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+        free_before = torch.cuda.mem_get_info(dev)[0]
+        step()
         torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info(dev)[0]
         extra.append(torch.cuda.max_memory_allocated() - base)
+        assert free_after == free_before, (N, free_before - free_after)
         assert ws.numel() == 4 * 4 * N
     # the library itself allocates nothing
     assert extra == [0, 0, 0]
