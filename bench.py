@@ -421,10 +421,14 @@ def workload_config(w, causal):
 
 KERNELS = ["fwd", "bwd_pre", "bwd_dq", "bwd_dkdv"]
 
-# MUFU (special-function unit) rate of ex2: 16 results per clock per SM, the
-# throughput table of the CUDA C++ programming guide for compute capability
-# 10.x; the peak is that x SMs x the SM clock (derived, not measured).
-MUFU_EX2_PER_CLK_PER_SM = 16
+# MUFU (special-function unit) rate of ex2 on this part: 32 results per clock
+# per SM.  Derived from counters, not from a table: in ncu captures of the
+# step kernels the XU pipe's utilisation (sm__inst_executed_pipe_xu, % of peak)
+# equals each kernel's ex2 count per second / (32 x SMs x SM clock) to within
+# 1.3 points (forward 26.6 % against 25.3 %, dQ 16.0 % against 15.6 %, dK/dV
+# 15.4 % against 15.0 %), i.e. ncu's peak is one warp-wide XU instruction per
+# clock per SM; the peak is that x SMs x the sampled SM clock.
+MUFU_EX2_PER_CLK_PER_SM = 32
 
 
 def kernel_work(w, causal):
@@ -668,8 +672,8 @@ def run_ours(args, world, rank, local):
         "bwd_hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "fwd_exp2_per_s": kernels["fwd"]["exp2_per_s"],
         "mufu_peak_exp2_per_s": mufu_peak,
-        "mufu_peak_derivation": (f"{MUFU_EX2_PER_CLK_PER_SM} ex2 per clock per SM (CUDA "
-                                 f"programming guide, compute capability 10.x) x {num_sms} SMs "
+        "mufu_peak_derivation": (f"{MUFU_EX2_PER_CLK_PER_SM} ex2 per clock per SM (the XU "
+                                 f"pipe's peak in ncu's counters on this part) x {num_sms} SMs "
                                  f"x {sm_mhz:.0f} MHz (median SM clock in the timed region)"),
         "host_enqueue_us_per_step": enqueue_us,
         "device_us_per_step": ms_per_step * 1e3,
@@ -731,7 +735,9 @@ def run_ours(args, world, rank, local):
             e2e_step(i)
         plan.wait()
         est = (time.perf_counter() - t0) / n_warm
-        n_e2e = int(min(E2E_MAX_STEPS, max(E2E_MIN_STEPS, math.ceil(E2E_MIN_SECONDS / est))))
+        # the warm-up steps run slower than the steady state: aim 50 % above
+        n_e2e = int(min(E2E_MAX_STEPS,
+                        max(E2E_MIN_STEPS, math.ceil(1.5 * E2E_MIN_SECONDS / est))))
         torch.cuda.synchronize(dev)
         barrier(world)
         t0 = time.perf_counter()
