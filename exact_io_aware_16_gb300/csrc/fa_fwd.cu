@@ -37,13 +37,10 @@
 // the other way round.  Committing S_g(j+1) also guarantees that PV_g(j) has
 // completed, so a warpgroup that has seen its scores may rescale O at once.
 //
-// Warp roles (384 threads): warps 0-3 tile 0 and warps 4-7 tile 1
+// Warp roles (320 threads): warps 0-3 tile 0 and warps 4-7 tile 1
 // (softmax / correction / epilogue; thread t <-> row t <-> TMEM lane t),
-// warp 8 TMA producer, warp 9 TMEM allocator and MMA issuer, warps 10-11
-// idle (they complete the role warpgroup, whose registers go to the softmax
-// warpgroups: 216 per thread there, 64 in the role warpgroup).
+// warp 8 TMA producer, warp 9 TMEM allocator and MMA issuer.
 #include <algorithm>
-#include <atomic>
 #include <mutex>
 #include <cstdint>
 #include <cuda.h>
@@ -68,22 +65,9 @@ __device__ unsigned int g_fwd_sched[kSchedSlots][2];
 constexpr int kItemRing = 4;  // claimed items in flight between the roles of a CTA
 
 
-// Warps 0-7: the two softmax warpgroups; warps 8-11: the role warpgroup
-// (warp 8 TMA, warp 9 TMEM allocation and MMA issue, warps 10-11 idle, so
-// that the role warps form a whole warpgroup for setmaxnreg).  At launch every
-// thread gets kLaunchRegs (three warps per SM sub-partition: 3 x 32 x 168 of
-// its 16,384 registers); the role warpgroup then drops to kRoleRegs and the
-// softmax warpgroups rise to kSoftmaxRegs, which the released registers cover.
-constexpr int kFwdThreads = 384;
+constexpr int kFwdThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kLaunchRegs = 168;
-constexpr int kRoleRegs = 64;
-constexpr int kSoftmaxRegs = 216;
-static_assert(256 * kSoftmaxRegs + 128 * kRoleRegs <= kFwdThreads * kLaunchRegs,
-              "register split exceeds the CTA's launch allocation");
-static_assert(2 * 32 * kSoftmaxRegs + 32 * kRoleRegs <= 16384,
-              "register split exceeds one SM sub-partition");
 constexpr int kStages = 2;
 
 // Ring slot and phase parity of the K / V tile at ring position pos >= 0
@@ -282,10 +266,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     return bars->item_ring[t % kItemRing];
   };
 
-  // Each role's code sits inside the branch that sets its register budget, so
-  // that the compiler allocates it within that budget.
-  if (warp >= kTmaWarp) {
-  setmaxnreg_dec<kRoleRegs>();
   if (warp == kTmaWarp) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -477,9 +457,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       umma_commit(&bars->drain);
     }
     __syncwarp();
-  }
   } else {
-    setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------ softmax warpgroups
     const int g = warp >> 2;           // which query tile of the pair
     const int t = threadIdx.x & 127;   // row within the tile, TMEM lane
@@ -568,8 +546,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // row sum adds each pair (p0 + p1) into partial sum (c / 2) % 4, x for
         // even c and y for odd c.  Two pairs at a time, with packed fma / add
         // (each lane rounded as the scalar op, so the sums are the same bit
-        // for bit).
-        constexpr bool kPairs = true;
+        // for bit), except in the persistent causal d = 128 kernel, whose item
+        // state leaves no registers for them (it spilled and ran 8 % slower at
+        // N = 2048; the dropout kernels spill a little too but gain 2.5 %).
+        constexpr bool kPairs = !(PERSIST && CAUSAL && D == 128);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           float p[4];
@@ -652,8 +632,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float inv_l =
           l_run > 0.0f ? (DROPOUT ? drop.rs : 1.0f) * (FP8 ? o_scale : 1.0f) / l_run : 0.0f;
       // Rows of this lane's 4-lane group are stored together, row by row (32
-      // columns at a time).
-      constexpr bool kGroupStore = true;
+      // columns at a time: the softmax warps' registers are scarce).  The
+      // persistent causal kernel, which carries its item state across the
+      // epilogue, has no registers left for the transpose and stores its own
+      // row (measured: the transpose there spills and costs 7 % at N = 2048).
+      constexpr bool kGroupStore = !(PERSIST && CAUSAL);
       const int r0 = kGroupStore ? row - (lane & 3) : row;
       const int grp_rows = min(kGroupStore ? 4 : 1, N - r0);
       __nv_bfloat16* ogrp = o + (static_cast<size_t>(bh) * N + (grp_rows > 0 ? r0 : 0)) * D;
@@ -745,17 +728,6 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   constexpr uint32_t smem = FwdLayout<D, FP8 ? 1 : 2>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // The setmaxnreg split draws on the registers the CTA is launched with:
-  // refuse to launch (rather than let setmaxnreg.inc wait forever) unless the
-  // compiled kernel's per-thread count covers it.  Checked once per instance.
-  static std::atomic<int> regs_ok{0};  // 0 unknown, 1 ok, 2 too few
-  if (regs_ok.load(std::memory_order_relaxed) == 0) {
-    cudaFuncAttributes fattr;
-    if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
-    const bool ok = fattr.numRegs * kFwdThreads >= 256 * kSoftmaxRegs + 128 * kRoleRegs;
-    regs_ok.store(ok ? 1 : 2, std::memory_order_relaxed);
-  }
-  if (regs_ok.load(std::memory_order_relaxed) != 1) return cudaErrorInvalidConfiguration;
   const long long nq = (a.N + kTileM - 1) / kTileM;
   const long long items = (nq + 1) / 2 * a.BH;
   if (items > 0x7fffffffll) return cudaErrorInvalidValue;

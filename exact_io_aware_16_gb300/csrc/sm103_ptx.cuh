@@ -382,22 +382,6 @@ __device__ __forceinline__ void store_rows(uint32_t (&w)[4 * G], __nv_bfloat16* 
           make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// Per-thread register budget of the calling warpgroup (all four warps of a
-// warpgroup execute the same one): dec hands registers back to the CTA's pool,
-// inc waits until the pool holds enough for the warpgroup.  The pool is what
-// the CTA was launched with (threads x registers per thread at launch), so
-// the launcher must check that the budgets of all warpgroups fit in it.
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register budget");
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register budget");
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Named barrier among `nthreads` threads (a multiple of 32) of this CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
