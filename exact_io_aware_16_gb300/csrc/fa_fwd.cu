@@ -12,11 +12,13 @@
 //     units of the scaled scores) and running sum l, writes
 //     P~ = 2^(s*scale*log2e - m) as bf16 back over its score row, and
 //     rescales the O accumulator by alpha = 2^(m_old - m_new).  The running max
-//     is only moved when a row's block max exceeds it by more than 2^8
-//     (kLazyRescaleLog2): until then P~ <= 2^8 against the stale max, and since
-//     O and l are scaled by the same factor, O / l is unchanged.  beta of the
-//     page is folded in by exponentiating against the current max directly
-//     (the "l_new" formula of the mentria page).
+//     is moved lazily: a tile's exponentials are first taken against the
+//     current running max, and only when some row's P~ would exceed a bound
+//     (2^16 for bf16 P~, 2^7 for e4m3) is the tile redone against a new max
+//     (moved when the block max exceeds the running max by more than 8, log2
+//     units); since O and l carry the same factor, O / l is unchanged.  beta
+//     of the page is folded in by exponentiating against the current max
+//     directly (the "l_new" formula of the mentria page).
 //   * O += P~ V_j is a tcgen05.mma with the P~ operand read from tensor
 //     memory and V from shared memory; O stays in tensor memory (fp32).
 //   * 06:52-07:24: at the end only O = O_acc / l (bf16) and one fp32
@@ -80,6 +82,15 @@ __device__ __forceinline__ uint32_t ring_phase(int pos) {
 }
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLazyRescaleLog2 = 8.0f;
+// A speculative tile (exponentials against the running max, before the block
+// max is known) is accepted when every row's sum of P~ is at most this bound,
+// so that every P~ is too.  e4m3 P~ must stay below 448: 2^7.  bf16 P~ and
+// the fp32 O and l accumulators are unharmed by P~ up to 2^16 (bf16 rounding
+// is relative, and O and l carry the same factor), so a bf16 tile is accepted
+// up to 2^16; a row's running max then trails its true max by at most 16
+// (log2) instead of 8, and O / l is the same up to rounding.
+constexpr float kSpeculateSumBoundF8 = 128.0f;
+constexpr float kSpeculateSumBound = 65536.0f;
 
 // EB: bytes per element of Q, K, V (2: bf16, 1: e4m3).  A tile is 128 rows;
 // every 128-byte run of a row is one swizzled TMA box column ("chunk").
@@ -502,103 +513,133 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       tc_fence_after_sync();
       uint32_t sr[128];
-      tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      tmem_ld_wait();
-      reg_pin(sr);
       const int kv0 = kv_of(j) * kTileN;
       // a key tile this query tile does not keep: every score is masked
       const bool keep = !SPARSE || ((list[j] >> (14 + g)) & 1);
       const bool need_mask = !keep || (CAUSAL && kv0 + kTileN - 1 > q0) || (kv0 + kTileN > N);
-      if (need_mask) {
-        const int lim_causal = CAUSAL ? (row - kv0) : 0x7fffffff;  // col index <= lim visible
-        const int lim_n = N - 1 - kv0;
-        const int lim = keep ? (lim_causal < lim_n ? lim_causal : lim_n) : -1;
+      // this row's 128 scores from tensor memory, masked where needed
+      auto load_scores = [&]() {
+        tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_ld_wait();
+        reg_pin(sr);
+        if (need_mask) {
+          const int lim_causal = CAUSAL ? (row - kv0) : 0x7fffffff;  // col index <= lim visible
+          const int lim_n = N - 1 - kv0;
+          const int lim = keep ? (lim_causal < lim_n ? lim_causal : lim_n) : -1;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      const float m_blk = row_max128(sr) * scale_log2;
-      // move the running max only when some row of the warp needs it
-      const bool move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
-      float alpha = 1.0f;
-      if (move) {
-        const float m_new = fmaxf(m_run, m_blk);
-        alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      // exponent arguments and row sums two lanes at a time (packed fp32 FMA / add)
-      const float2 sc2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-m_use, -m_use);
-      float2 sp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};  // partial row sums
-      if (FP8) {
-        // P~ as e4m3, four per word: quad c overwrites sr[c], already consumed
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 x01 = __ffma2_rn(
-              make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), sc2, nm2);
-          const float2 x23 = __ffma2_rn(
-              make_float2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])), sc2,
-              nm2);
-          const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-          const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-          sp[(2 * c) & 3] = __fadd2_rn(sp[(2 * c) & 3], p01);
-          sp[(2 * c + 1) & 3] = __fadd2_rn(sp[(2 * c + 1) & 3], p23);
-          sr[c] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
+          for (int c = 0; c < 128; ++c)
+            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
         }
-      } else {
-        // P~ packed in place: pair c overwrites sr[c], already consumed.  The
-        // row sum adds each pair (p0 + p1) into partial sum (c / 2) % 4, x for
-        // even c and y for odd c.  Two pairs at a time, with packed fma / add
-        // (each lane rounded as the scalar op, so the sums are the same bit
-        // for bit), except in the persistent causal d = 128 kernel, whose item
-        // state leaves no registers for them (it spilled and ran 8 % slower at
-        // N = 2048; the dropout kernels spill a little too but gain 2.5 %).
-        constexpr bool kPairs = !(PERSIST && CAUSAL && D == 128);
+      };
+      load_scores();
+      // Once the rows have a finite running max, the tile's exponentials are
+      // first taken against it without looking at the block max (the row max
+      // is off the common path).  If every row's sum of P~ is then within the
+      // bound (kSpeculateSumBound, e4m3: kSpeculateSumBoundF8), so is every
+      // P~, and the tile stands.  Otherwise (rare) it is redone the exact way:
+      // scores reloaded, block max, and the running max moved when some row's
+      // block max exceeds it by more than 8 (log2 units, kLazyRescaleLog2).
+      float sum = 0.0f;
+      // exponentials of this row's scores against the running max (P~ packed
+      // into sr) and their sum
+      auto exp_tile = [&]() {
+        const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+        // exponent arguments and row sums two lanes at a time (packed fp32 FMA / add)
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        float2 sp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};  // partial row sums
+        if (FP8) {
+          // P~ as e4m3, four per word: quad c overwrites sr[c], already consumed
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float p[4];
-          if (kPairs) {
-            const float2 x0 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
-            const float2 x1 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[2 * c + 2]), __uint_as_float(sr[2 * c + 3])), sc2,
+          for (int c = 0; c < 32; ++c) {
+            const float2 x01 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])), sc2, nm2);
+            const float2 x23 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])), sc2,
                 nm2);
-            p[0] = ex2_approx(x0.x);
-            p[1] = ex2_approx(x0.y);
-            p[2] = ex2_approx(x1.x);
-            p[3] = ex2_approx(x1.y);
-            const float2 pair = __fadd2_rn(make_float2(p[0], p[2]), make_float2(p[1], p[3]));
-            sp[(c >> 1) & 3] = __fadd2_rn(sp[(c >> 1) & 3], pair);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              p[e] = ex2_approx(fmaf(__uint_as_float(sr[2 * c + e]), scale_log2, -m_use));
-            sp[(c >> 1) & 3].x += p[0] + p[1];
-            sp[(c >> 1) & 3].y += p[2] + p[3];
+            const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+            const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+            sp[(2 * c) & 3] = __fadd2_rn(sp[(2 * c) & 3], p01);
+            sp[(2 * c + 1) & 3] = __fadd2_rn(sp[(2 * c + 1) & 3], p23);
+            sr[c] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
           }
+        } else {
+          // P~ packed in place: pair c overwrites sr[c], already consumed.  The
+          // row sum adds each pair (p0 + p1) into partial sum (c / 2) % 4, x for
+          // even c and y for odd c.  Two pairs at a time, with packed fma / add
+          // (each lane rounded as the scalar op, so the sums are the same bit
+          // for bit), except in the persistent causal d = 128 kernel, whose item
+          // state leaves no registers for them (it spilled and ran 8 % slower at
+          // N = 2048; the dropout kernels spill a little too but gain 2.5 %).
+          constexpr bool kPairs = !(PERSIST && CAUSAL && D == 128);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float p0 = p[2 * h], p1 = p[2 * h + 1];
-            const int cc = c + h;
-            if (DROPOUT) {
-              const uint32_t bits = kb[cc >> 4] >> ((2 * cc) & 31);
-              sr[cc] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+          for (int c = 0; c < 64; c += 2) {
+            float p[4];
+            if (kPairs) {
+              const float2 x0 = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+              const float2 x1 = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[2 * c + 2]), __uint_as_float(sr[2 * c + 3])), sc2,
+                  nm2);
+              p[0] = ex2_approx(x0.x);
+              p[1] = ex2_approx(x0.y);
+              p[2] = ex2_approx(x1.x);
+              p[3] = ex2_approx(x1.y);
+              const float2 pair = __fadd2_rn(make_float2(p[0], p[2]), make_float2(p[1], p[3]));
+              sp[(c >> 1) & 3] = __fadd2_rn(sp[(c >> 1) & 3], pair);
             } else {
-              sr[cc] = pack_bf16x2(p0, p1);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                p[e] = ex2_approx(fmaf(__uint_as_float(sr[2 * c + e]), scale_log2, -m_use));
+              sp[(c >> 1) & 3].x += p[0] + p[1];
+              sp[(c >> 1) & 3].y += p[2] + p[3];
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float p0 = p[2 * h], p1 = p[2 * h + 1];
+              const int cc = c + h;
+              if (DROPOUT) {
+                const uint32_t bits = kb[cc >> 4] >> ((2 * cc) & 31);
+                sr[cc] = pack_bf16x2((bits & 1u) ? p0 : 0.0f, (bits & 2u) ? p1 : 0.0f);
+              } else {
+                sr[cc] = pack_bf16x2(p0, p1);
+              }
             }
           }
         }
+        const float2 s01 = __fadd2_rn(sp[0], sp[1]);
+        const float2 s23 = __fadd2_rn(sp[2], sp[3]);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        sum = s4.x + s4.y;
+      };
+      bool move = false;
+      float alpha = 1.0f;
+      bool exact = !__all_sync(0xffffffffu, m_run != -INFINITY);
+      if (!exact) {
+        exp_tile();
+        // speculation held unless some row's sum exceeds the bound (or is not finite)
+        constexpr float kBound = FP8 ? kSpeculateSumBoundF8 : kSpeculateSumBound;
+        if (__any_sync(0xffffffffu, !(sum <= kBound))) {
+          load_scores();  // the speculative pass overwrote sr with P~
+          exact = true;
+        }
       }
-      const float2 s01 = __fadd2_rn(sp[0], sp[1]);
-      const float2 s23 = __fadd2_rn(sp[2], sp[3]);
-      const float2 s4 = __fadd2_rn(s01, s23);
-      const float sum = s4.x + s4.y;
+      if (exact) {
+        const float m_blk = row_max128(sr) * scale_log2;
+        // move the running max only when some row of the warp needs it
+        move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
+        if (move) {
+          const float m_new = fmaxf(m_run, m_blk);
+          alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        exp_tile();
+      }
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       if (!FP8) tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       if (move && j > 0) {
