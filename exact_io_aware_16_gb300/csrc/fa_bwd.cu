@@ -377,7 +377,7 @@ __device__ __forceinline__ void store_acc_half(uint32_t addr, float mul, __nv_bf
 // dV = rs (P o Z)^T dO and dS = P o (rs Z o dP - D); P itself (undropped)
 // stays in registers for dS, P o Z goes to the dV product, rs is applied when
 // dV is stored.  The keep bits of a key row come transposed from the
-// generator's row-major counters (keep_byte_t).
+// generator's row-major counters (keep_word_t).
 template <int D, bool CAUSAL, bool SPARSE, bool DROPOUT, bool PERSIST>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq,
@@ -584,11 +584,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t kb[2] = {0u, 0u};
       if (DROPOUT) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          kb[u >> 2] |= keep_byte_t(drop, static_cast<uint32_t>(krow),
-                                    static_cast<uint32_t>(q0) + col0 + 8u * u,
-                                    static_cast<uint32_t>(bh), lane)
-                        << (8 * (u & 3));
+        for (int w = 0; w < 2; ++w)
+          kb[w] = keep_word_t(drop, static_cast<uint32_t>(krow),
+                              static_cast<uint32_t>(q0) + col0 + 32u * w,
+                              static_cast<uint32_t>(bh), lane);
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!bwd_warp_wait(&bars->s_full, (nb + n) & 1, bars, 0x301)) {

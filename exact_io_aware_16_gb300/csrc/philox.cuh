@@ -75,22 +75,29 @@ __device__ __forceinline__ uint32_t keep_byte(const DropArgs& dr, uint32_t jg, u
 
 // Keep bits, transposed across a warp: lane L holds key row jrow (eight
 // consecutive lanes hold eight consecutive keys starting at a multiple of 8)
-// and wants the decisions for query rows i0 .. i0+7.  Each lane computes one
-// counter (its octet's key group, row i0 + L % 8); eight ballots, one per key
-// of the group, hand every lane its own key's column of the 8 x 8 block.
-// Returns the keep bits of rows i0 + r as bits r = 0..7.  All 32 lanes must
+// and wants the decisions for query rows i0 .. i0+31.  Each lane computes four
+// counters (its octet's key group, rows i0 + 8u + L % 8 for u = 0..3): byte u
+// of its word is then row L % 8 of an 8 x 8 bit block (bit c: key 8m + c).
+// Three XOR-shuffle butterfly stages transpose all four blocks of the octet at
+// once (stage b swaps the off-diagonal b x b sub-blocks between lanes b
+// apart; the masks keep the bytes apart), leaving in byte u of lane L the
+// column L % 8 of block u: bit k = row i0 + 8u + k of this lane's key.
+// Returns the keep bits of rows i0 + t as bits t = 0..31.  All 32 lanes must
 // call it together.
-__device__ __forceinline__ uint32_t keep_byte_t(const DropArgs& dr, uint32_t jrow, uint32_t i0,
+__device__ __forceinline__ uint32_t keep_word_t(const DropArgs& dr, uint32_t jrow, uint32_t i0,
                                                 uint32_t bh, int lane) {
   const uint32_t r = static_cast<uint32_t>(lane) & 7u;
-  const uint32_t mine = keep_byte(dr, jrow >> 3, i0 + r, bh);  // row i0 + r, keys of the octet
-  uint32_t col = 0;
+  uint32_t x = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const uint32_t b = __ballot_sync(0xffffffffu, (mine >> e) & 1u);  // bit 8m + r: row r, key e
-    if (static_cast<uint32_t>(e) == r) col = b;
+  for (uint32_t u = 0; u < 4; ++u) x |= keep_byte(dr, jrow >> 3, i0 + 8u * u + r, bh) << (8 * u);
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    const int b = 4 >> s;
+    const uint32_t lo = s == 0 ? 0x0F0F0F0Fu : (s == 1 ? 0x33333333u : 0x55555555u);
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, b);
+    x = (lane & b) ? ((x & ~lo) | ((y >> b) & lo)) : ((x & lo) | ((y << b) & ~lo));
   }
-  return (col >> (static_cast<uint32_t>(lane) & ~7u)) & 0xFFu;
+  return x;
 }
 
 }  // namespace fa
