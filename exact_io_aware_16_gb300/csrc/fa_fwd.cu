@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       constexpr uint32_t idesc_f8 = idesc_e4m3_f32(128, 128);
-      // S_g = Q_g K^T from the K tile at ring position pos
+      // S_g = Q_g K^T from the K tile at ring position pos (no commit)
       auto issue_s = [&](int g, int pos) {
         const uint32_t kbase = sK + ring_slot(pos) * L::kTileBytes;
         const uint32_t qbase = sQ + g * L::kTileBytes;
@@ -374,9 +374,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
           }
         }
-        umma_commit(&bars->s_full[g]);
       };
-      // O_g (+)= P_g V from the V tile at ring position pos; `first` starts O afresh
+      // O_g (+)= P_g V from the V tile at ring position pos; `first` starts O
+      // afresh (no commit)
       auto issue_pv = [&](int g, int pos, bool first) {
         const uint32_t vbase = sV + ring_slot(pos) * L::kTileBytes;
         if (FP8) {  // A = P~ e4m3, 8 tensor-memory columns per 32 keys; B = V^T K-major
@@ -392,11 +392,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     sdesc_sw128(vbase + kk * 2048, 16384, 1024), idesc_pv,
                     (!first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars->pv_done[g]);
       };
-      // one item: t = items before it in this CTA, kvb = its first K / V ring
+      // One item: t = items before it in this CTA, kvb = its first K / V ring
       // position, base0 / base1 = tiles each softmax warpgroup finished before
       // it.  Returns false after a pipeline timeout.
+      //
+      // For key tile j the products go out in two bursts, PV0_j S0_{j+1} and
+      // PV1_j S1_{j+1}, each preceded by the waits for everything it reads,
+      // so that no wait sits between the two products of a burst: a blocking
+      // wait of this thread between products leaves the tensor core idle
+      // after the earlier ones complete.  Group 1's P is usually ready by the
+      // time group 0's burst has gone out, so it is first tested without
+      // blocking, and when it is ready its burst follows at once.
       auto mma_item = [&](const int item, const int t, const int kvb, const int base0,
                           const int base1) -> bool {
         const int n0 = item_n(item, 0), n1 = item_n(item, 1);
@@ -406,7 +413,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!ok) return false;
         tc_fence_after_sync();
         issue_s(0, kvb);
+        umma_commit(&bars->s_full[0]);
         issue_s(1, kvb);
+        umma_commit(&bars->s_full[1]);
         umma_commit(&bars->k_empty[ring_slot(kvb)]);
         for (int j = 0; j < n1; ++j) {
           const int pos = kvb + j;
@@ -414,36 +423,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t ph = ring_phase(pos);
           const int sn = ring_slot(pos + 1);
           const uint32_t phn = ring_phase(pos + 1);
-          bool v_ready = false, k_next_ready = false;
+          bool pre1 = false;
           if (j < n0) {
+            // burst of group 0: P0_j, V_j, and K_{j+1} for S0_{j+1} (or for
+            // S1_{j+1} alone when group 0 ends here)
             ok = mma_wait(&bars->p_ready[0], (base0 + j) & 1, bars, 0x203) &&
                  mma_wait(&bars->v_full[s], ph, bars, 0x204) &&
-                 (j > 0 || t == 0 || mma_wait(&bars->o_free[0], (t - 1) & 1, bars, 0x209));
+                 (j > 0 || t == 0 || mma_wait(&bars->o_free[0], (t - 1) & 1, bars, 0x209)) &&
+                 (j + 1 >= n1 || mma_wait(&bars->k_full[sn], phn, bars, 0x205));
             if (!ok) break;
-            v_ready = true;
             tc_fence_after_sync();
             issue_pv(0, pos, j == 0);
-            if (j + 1 < n0) {
-              if (!mma_wait(&bars->k_full[sn], phn, bars, 0x205)) { ok = false; break; }
-              k_next_ready = true;
-              tc_fence_after_sync();
-              issue_s(0, pos + 1);
-            }
+            umma_commit(&bars->pv_done[0]);
+            if (j + 1 < n0) issue_s(0, pos + 1);
+            pre1 = mbar_test_wait(&bars->p_ready[1], (base1 + j) & 1) &&
+                   (j > 0 || t == 0 || mbar_test_wait(&bars->o_free[1], (t - 1) & 1));
+            if (j + 1 < n0) umma_commit(&bars->s_full[0]);
           }
-          ok = mma_wait(&bars->p_ready[1], (base1 + j) & 1, bars, 0x206) &&
-               (v_ready || mma_wait(&bars->v_full[s], ph, bars, 0x207)) &&
-               (j > 0 || t == 0 || mma_wait(&bars->o_free[1], (t - 1) & 1, bars, 0x20a));
-          if (!ok) break;
+          // burst of group 1: P1_j (V_j and K_{j+1} are in when group 0 had
+          // this tile)
+          if (!pre1) {
+            ok = mma_wait(&bars->p_ready[1], (base1 + j) & 1, bars, 0x206) &&
+                 (j < n0 || mma_wait(&bars->v_full[s], ph, bars, 0x207)) &&
+                 (j > 0 || t == 0 || mma_wait(&bars->o_free[1], (t - 1) & 1, bars, 0x20a)) &&
+                 (j < n0 || j + 1 >= n1 || mma_wait(&bars->k_full[sn], phn, bars, 0x208));
+            if (!ok) break;
+          }
           tc_fence_after_sync();
           issue_pv(1, pos, j == 0);
           umma_commit(&bars->v_empty[s]);
+          if (j + 1 < n1) issue_s(1, pos + 1);
+          umma_commit(&bars->pv_done[1]);
           if (j + 1 < n1) {
-            if (!k_next_ready && !mma_wait(&bars->k_full[sn], phn, bars, 0x208)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            issue_s(1, pos + 1);
+            umma_commit(&bars->s_full[1]);
             umma_commit(&bars->k_empty[sn]);
           }
         }
