@@ -470,20 +470,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t sV = smem_u32(smem + L::kRes1);
       auto sQ = [&](int pos) { return smem_u32(smem + L::kStr0 + ring_slot(pos) * L::kTileBytes); };
       auto sdO = [&](int pos) { return smem_u32(smem + L::kStr1 + ring_slot(pos) * L::kTileBytes); };
-      // S^T = K Q^T and dP^T = V dO^T of the streamed tile at ring position pos
+      // S^T = K Q^T and dP^T = V dO^T of the streamed tile at ring position
+      // pos (the commit is the caller's)
       auto issue_s = [&](int pos) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + L::kSCol, kmajor_desc(sK, kk), kmajor_desc(sQ(pos), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full);
       };
       auto issue_dp = [&](int pos) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + L::kDPCol, kmajor_desc(sV, kk), kmajor_desc(sdO(pos), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(&bars->dp_full);
       };
       // one item: t = items before it in this CTA, sb = ring position of its
       // first streamed tile, nb = steps before it (barrier phases)
@@ -496,11 +495,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) return false;
         tc_fence_after_sync();
         issue_s(sb);
+        umma_commit(&bars->s_full);
         issue_dp(sb);
+        umma_commit(&bars->dp_full);
         // order per step: dV_n, S^T_{n+1}, dK_n, dP^T_{n+1}, so that the exps of
-        // step n+1 overlap dK_n and dP^T_{n+1} on the tensor core
+        // step n+1 overlap dK_n and dP^T_{n+1} on the tensor core.  They go out
+        // as two bursts (dV_n S^T_{n+1}, dK_n dP^T_{n+1}) with the waits for
+        // what a burst reads ahead of it where the barriers have already
+        // completed: a blocking wait of this thread between two products
+        // leaves the tensor core idle once the earlier one completes.
         for (int n = 0; n < n_iters; ++n) {
           const int pos = sb + n;
+          const bool more = n + 1 < n_iters;
           // dV += P^T dO_n   (A = P^T bf16 in TMEM, B = dO_n MN-major, K = 128 queries);
           // the first one of an item overwrites the accumulators the previous
           // item's epilogue read
@@ -510,23 +516,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ok = false;
             break;
           }
+          const bool next_in =
+              !more || mbar_test_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1));
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tmem + L::kAcc0, tmem + L::kSCol + packed_a_col(kk), mnmajor_desc(sdO(pos), kk),
                     idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-          const bool more = n + 1 < n_iters;
           if (more) {
-            if (!mbar_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1),
-                           &bars->abort_flag, &g_bwd_error, 0x205)) {
-              ok = false;
-              break;
+            if (!next_in) {
+              if (!mbar_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1),
+                             &bars->abort_flag, &g_bwd_error, 0x205)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
             }
-            tc_fence_after_sync();
             issue_s(pos + 1);
           }
           // dK += dS^T Q_n   (A = dS^T bf16 in TMEM, B = Q_n MN-major)
-          if (!mbar_wait(&bars->ds_ready, (nb + n) & 1, &bars->abort_flag, &g_bwd_error, 0x204)) {
+          const bool ds_in = mbar_test_wait(&bars->ds_ready, (nb + n) & 1);
+          if (more) umma_commit(&bars->s_full);
+          if (!ds_in &&
+              !mbar_wait(&bars->ds_ready, (nb + n) & 1, &bars->abort_flag, &g_bwd_error, 0x204)) {
             ok = false;
             break;
           }
@@ -536,7 +548,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_ts(tmem + L::kAcc1, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sQ(pos), kk),
                     idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars->str_empty[ring_slot(pos)]);
-          if (more) issue_dp(pos + 1);
+          if (more) {
+            issue_dp(pos + 1);
+            umma_commit(&bars->dp_full);
+          }
         }
         if (ok) umma_commit(&bars->acc_done);
         umma_commit(&bars->res_empty);  // K, V free once the products above complete
@@ -842,19 +857,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto sK = [&](int pos) { return smem_u32(smem + L::kStr0 + ring_slot(pos) * L::kTileBytes); };
       auto sV = [&](int pos) { return smem_u32(smem + L::kStr1 + ring_slot(pos) * L::kTileBytes); };
       // S = Q K^T  and  dP = dO V^T of the streamed tile at ring position pos
+      // (the commit is the caller's)
       auto issue_s = [&](int pos) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + L::kSCol, kmajor_desc(sQ, kk), kmajor_desc(sK(pos), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full);
       };
       auto issue_dp = [&](int pos) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV(pos), kk), idesc_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(&bars->dp_full);
       };
       // one item: t = items before it in this CTA, sb = ring position of its
       // first streamed tile (= steps before it: barrier phases)
@@ -867,10 +881,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) return false;
         tc_fence_after_sync();
         issue_s(sb);
+        umma_commit(&bars->s_full);
         issue_dp(sb);
-        // order per step: B_n, S_{n+1}, dQ~_n, dP_{n+1}
+        umma_commit(&bars->dp_full);
+        // order per step: B_n, S_{n+1}, dQ~_n, dP_{n+1}, as two bursts with the
+        // waits ahead of them where the barriers have already completed (as in
+        // the dK/dV kernel)
         for (int n = 0; n < n_iters; ++n) {
           const int pos = sb + n;
+          const bool more = n + 1 < n_iters;
           // B += P K_n   (A = P bf16 in TMEM over S, B = K_n MN-major); the
           // first one of an item overwrites the accumulators the previous
           // item's epilogue read
@@ -880,23 +899,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ok = false;
             break;
           }
+          const bool next_in =
+              !more || mbar_test_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1));
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tmem + kB, tmem + L::kSCol + packed_a_col(kk), mnmajor_desc(sK(pos), kk),
                     idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-          const bool more = n + 1 < n_iters;
           if (more) {
-            if (!mbar_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1),
-                           &bars->abort_flag, &g_bwd_error, 0x215)) {
-              ok = false;
-              break;
+            if (!next_in) {
+              if (!mbar_wait(&bars->str_full[ring_slot(pos + 1)], ring_phase(pos + 1),
+                             &bars->abort_flag, &g_bwd_error, 0x215)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
             }
-            tc_fence_after_sync();
             issue_s(pos + 1);
           }
           // dQ~ += dS~ K_n   (A = dS~ bf16 in TMEM over dP)
-          if (!mbar_wait(&bars->ds_ready, pos & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
+          const bool ds_in = mbar_test_wait(&bars->ds_ready, pos & 1);
+          if (more) umma_commit(&bars->s_full);
+          if (!ds_in &&
+              !mbar_wait(&bars->ds_ready, pos & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
             ok = false;
             break;
           }
@@ -906,7 +931,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_ts(tmem + kDQ, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sK(pos), kk),
                     idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars->str_empty[ring_slot(pos)]);
-          if (more) issue_dp(pos + 1);
+          if (more) {
+            issue_dp(pos + 1);
+            umma_commit(&bars->dp_full);
+          }
         }
         if (ok) umma_commit(&bars->acc_done);
         umma_commit(&bars->res_empty);  // Q, dO free once the products above complete
