@@ -740,11 +740,16 @@ def run_ours(args, world, rank, local):
                         max(E2E_MIN_STEPS, math.ceil(1.5 * E2E_MIN_SECONDS / est))))
         torch.cuda.synchronize(dev)
         barrier(world)
+        eclk = ClockSampler(local)
+        eclk.start()
+        eclk.mark_load()
         t0 = time.perf_counter()
         for i in range(n_e2e):
             e2e_step(i)
         plan.wait()
         e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world) / n_e2e
+        eclk.mark_done()
+        e_clk = eclk.stop()
         plan.close()
         h2d = sum(t.numel() * t.element_size() for t in sets[0][0])
         d2h = sum(t.numel() * t.element_size() for t in sets[0][1])
@@ -754,6 +759,10 @@ def run_ours(args, world, rank, local):
                "steps": n_e2e, "seconds": n_e2e * e_ms * 1e-3,
                "how": "fa_host_step (C ABI, pinned host buffers, two-slot copy/compute "
                       "pipeline), host wall clock"}
+        if e_clk:  # the SM clock the kernels ran at here (the power cap lowers it in long runs)
+            e2e["clocks"] = {k: e_clk[k] for k in ("sm_mhz", "sm_mhz_min", "power_w_max",
+                                                    "reasons", "samples_under_load")
+                             if k in e_clk}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
