@@ -588,6 +588,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int k0 = kt * 128;
     const int krow = k0 + tr;
     const int n_iters = item_iters(item);
+    // the generator's products that depend on this key row's counter words alone
+    const PhiloxCol pcol = DROPOUT ? philox_col_init(drop, static_cast<uint32_t>(krow) >> 3,
+                                                     static_cast<uint32_t>(bh))
+                                   : PhiloxCol{};
     for (int n = 0; n < n_iters; ++n) {
       const int it = SPARSE ? static_cast<int>(list[n]) : item_first(item) + n;
       const int q0 = it * 128;
@@ -600,9 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (DROPOUT) {
 #pragma unroll
         for (int w = 0; w < 2; ++w)
-          kb[w] = keep_word_t(drop, static_cast<uint32_t>(krow),
-                              static_cast<uint32_t>(q0) + col0 + 32u * w,
-                              static_cast<uint32_t>(bh), lane);
+          kb[w] = keep_word_t(drop, pcol, static_cast<uint32_t>(q0) + col0 + 32u * w, lane);
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!bwd_warp_wait(&bars->s_full, (nb + n) & 1, bars, 0x301)) {
@@ -970,6 +972,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool rvalid = row < N;
     const float lse2 = rvalid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : 0.0f;
     const float Dt = rvalid ? Dvec[static_cast<size_t>(bh) * N + row] : 0.0f;  // D~
+    // the generator's products that depend on this row's counter words alone
+    const PhiloxRow prow = DROPOUT ? philox_row_init(drop, static_cast<uint32_t>(row),
+                                                     static_cast<uint32_t>(bh))
+                                   : PhiloxRow{};
     // this half's part of the exact D = sum_j P_ij dP_ij (four partial sums)
     float2 dx2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     bool ok = true;
@@ -981,8 +987,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t jg0 = (static_cast<uint32_t>(kt_of(n)) * 128u + col0) >> 3;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          kb[u >> 2] |= keep_byte(drop, jg0 + u, static_cast<uint32_t>(row),
-                                  static_cast<uint32_t>(bh)) << (8 * (u & 3));
+          kb[u >> 2] |= keep_byte_row(drop, prow, jg0 + u) << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
       if (!bwd_warp_wait(&bars->s_full, (nb + n) & 1, bars, 0x311)) {

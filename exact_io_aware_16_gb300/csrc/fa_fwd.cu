@@ -495,6 +495,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int row = (2 * pair + g) * kTileM + t;
     const int nkv = item_n(item, g);
     const int q0 = (2 * pair + g) * kTileM;
+    // the generator's products that depend on this row's counter words alone
+    const PhiloxRow prow = DROPOUT ? philox_row_init(drop, static_cast<uint32_t>(row),
+                                                     static_cast<uint32_t>(bh))
+                                   : PhiloxRow{};
     float m_run = -INFINITY;  // running (lazily moved) max of s * scale * log2(e)
     float l_run = 0.0f;
     for (int j = 0; j < nkv; ++j) {
@@ -513,8 +517,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint32_t acc = 0;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            acc |= keep_byte(drop, jg0 + 4 * w + u, static_cast<uint32_t>(row),
-                             static_cast<uint32_t>(bh)) << (8 * u);
+            acc |= keep_byte_row(drop, prow, jg0 + 4 * w + u) << (8 * u);
           kb[0] = kb[1]; kb[1] = kb[2]; kb[2] = kb[3]; kb[3] = acc;
         }
         reg_pin(kb);  // drawn here, before the wait, not next to their use
