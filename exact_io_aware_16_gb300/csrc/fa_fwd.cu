@@ -634,18 +634,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool move = false;
       float alpha = 1.0f;
       bool exact = !__all_sync(0xffffffffu, m_run != -INFINITY);
-      if (!exact) {
-        exp_tile();
-        // speculation held unless some row's sum exceeds the bound (or is not finite)
-        constexpr float kBound = FP8 ? kSpeculateSumBoundF8 : kSpeculateSumBound;
-        if (__any_sync(0xffffffffu, !(sum <= kBound))) {
-          load_scores();  // the speculative pass overwrote sr with P~
-          exact = true;
-        }
-      }
-      if (exact) {
+      constexpr float kBound = FP8 ? kSpeculateSumBoundF8 : kSpeculateSumBound;
+      // the block max of the scores, and the running max moved when some row
+      // of the warp needs it
+      auto move_max = [&]() {
         const float m_blk = row_max128(sr) * scale_log2;
-        // move the running max only when some row of the warp needs it
         move = __any_sync(0xffffffffu, m_blk > m_run + kLazyRescaleLog2);
         if (move) {
           const float m_new = fmaxf(m_run, m_blk);
@@ -653,7 +646,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           l_run *= alpha;
           m_run = m_new;
         }
-        exp_tile();
+      };
+      if (DROPOUT || FP8 || SPARSE) {
+        // two copies of the exponential loop (the speculative and the exact
+        // pass); one shared copy in a loop, as below, measured slower here:
+        // 9 % with dropout (the keep bits live across it), 7.6 % for e4m3,
+        // 0.7 % block-sparse
+        if (!exact) {
+          exp_tile();
+          // speculation held unless some row's sum exceeds the bound (or is not finite)
+          if (__any_sync(0xffffffffu, !(sum <= kBound))) {
+            load_scores();  // the speculative pass overwrote sr with P~
+            exact = true;
+          }
+        }
+        if (exact) {
+          move_max();
+          exp_tile();
+        }
+      } else {
+        // one copy of the exponential loop, run once, or twice when the
+        // speculative pass fails (the smaller kernel spills less and ran 1-4 %
+        // faster)
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          if (exact) move_max();
+          exp_tile();
+          if (exact) break;
+          // speculation held unless some row's sum exceeds the bound (or is not finite)
+          if (!__any_sync(0xffffffffu, !(sum <= kBound))) break;
+          load_scores();  // the speculative pass overwrote sr with P~
+          exact = true;
+        }
       }
       tmem_st32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       if (!FP8) tmem_st32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
