@@ -48,7 +48,10 @@ __device__ unsigned int g_bwd_sched[kSchedSlots][2];
 constexpr int kItemRing = 4;  // claimed items in flight between the roles of a CTA
 
 constexpr int kBwdThreads = 320;
-constexpr int kStages = 2;
+constexpr int kStages = 2;  // streamed-tile ring at d = 128 (shared memory allows no more)
+// d = 64: a four-stage ring, where the scores of the next step are issued
+// before the current step's products and need their tiles a step earlier
+constexpr int kStages64 = 4;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 // ============================================================ D pre-pass
@@ -96,15 +99,16 @@ constexpr int kMmaWarp = 9;
 
 template <int D>
 struct BwdLayout {
+  static constexpr int kRing = D == 64 ? kStages64 : kStages;
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   // dkdv: K, V resident; Q, dO streamed.  dq: Q, dO resident; K, V streamed.
   static constexpr uint32_t kRes0 = 0;
   static constexpr uint32_t kRes1 = kRes0 + kTileBytes;
   static constexpr uint32_t kStr0 = kRes1 + kTileBytes;                // [stage] tiles
-  static constexpr uint32_t kStr1 = kStr0 + kStages * kTileBytes;      // [stage] tiles
-  static constexpr uint32_t kVec = kStr1 + kStages * kTileBytes;       // lse/D vectors
-  static constexpr uint32_t kBar = kVec + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kStr1 = kStr0 + kRing * kTileBytes;       // [stage] tiles
+  static constexpr uint32_t kVec = kStr1 + kRing * kTileBytes;         // lse/D vectors
+  static constexpr uint32_t kBar = kVec + kRing * 2 * 128 * 4;
   static constexpr uint32_t kList = kBar + 256;  // block-sparse tile list (uint16)
   static constexpr uint32_t kSmemUsed = kList + 2 * kMaxSparseTiles + 1024;
   // at least 116 KB, so two CTAs never share an SM (each takes all 512 TMEM columns)
@@ -114,6 +118,13 @@ struct BwdLayout {
   static constexpr uint32_t kDPCol = 128;  // dP (or dP^T); dS bf16 packed inside each half
   static constexpr uint32_t kAcc0 = 256;   // dV (dkdv) or dQ~ (dq)
   static constexpr uint32_t kAcc1 = 256 + D;  // dK (dkdv) or B = P K (dq)
+  // d = 64: the accumulators leave columns 384..511 free, a second score
+  // buffer: step g's scores (and P over them) sit in buffer g % 2, so the next
+  // step's score product need not wait for this step's P to be consumed
+  static constexpr bool kDoubleS = D == 64;
+  __host__ __device__ static constexpr uint32_t s_col(int step) {
+    return (kDoubleS && (step & 1)) ? 384u : kSCol;
+  }
 };
 
 struct BwdBars {
@@ -130,7 +141,40 @@ struct BwdBars {
   int abort_flag;
   int nlist;  // block-sparse: entries of the tile list
   int item_ring[kItemRing];  // claimed items (-1: no more)
+  // d = 64 only: ring stages 2 and 3, and the "scores ready" / "P ready"
+  // barriers of score buffer 1 (each buffer has its own: with step g + 1's
+  // scores issued before step g's P is consumed, one barrier could complete a
+  // second phase before the waiter of the first has seen it)
+  uint64_t str_full_hi[2], str_empty_hi[2];
+  uint64_t s_full_1, p_ready_1;
 };
+
+static_assert(sizeof(BwdBars) <= 256, "barrier block overruns its shared-memory slot");
+
+// Barriers of ring stage s, and of score buffer b, in a ring of R stages
+template <int R>
+__device__ __forceinline__ uint64_t* str_full_bar(BwdBars* b, int s) {
+  if constexpr (R == 2) return &b->str_full[s];
+  else return s < 2 ? &b->str_full[s] : &b->str_full_hi[s - 2];
+}
+template <int R>
+__device__ __forceinline__ uint64_t* str_empty_bar(BwdBars* b, int s) {
+  if constexpr (R == 2) return &b->str_empty[s];
+  else return s < 2 ? &b->str_empty[s] : &b->str_empty_hi[s - 2];
+}
+// step g's "scores ready" / "P ready" barrier and its parity
+template <bool DS>
+__device__ __forceinline__ uint64_t* s_full_bar(BwdBars* b, int g) {
+  if constexpr (DS) return (g & 1) ? &b->s_full_1 : &b->s_full;
+  else return &b->s_full;
+}
+template <bool DS>
+__device__ __forceinline__ uint64_t* p_ready_bar(BwdBars* b, int g) {
+  if constexpr (DS) return (g & 1) ? &b->p_ready_1 : &b->p_ready;
+  else return &b->p_ready;
+}
+template <bool DS>
+__host__ __device__ constexpr uint32_t s_parity(int g) { return DS ? ((g >> 1) & 1) : (g & 1); }
 
 // Adds `bytes` to the transaction count of the current phase of `bar`
 // without arriving (the arrival comes separately, after staged data).
@@ -140,12 +184,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Ring slot and phase parity of the streamed tile at ring position pos >= 0.
+// Ring slot and phase parity of the streamed tile at ring position pos >= 0
+// (R stages, a power of two; 2 unless stated).
+template <int R = kStages>
 __device__ __forceinline__ int ring_slot(int pos) {
-  return static_cast<int>(static_cast<unsigned>(pos) % kStages);
+  return static_cast<int>(static_cast<unsigned>(pos) % R);
 }
+template <int R = kStages>
 __device__ __forceinline__ uint32_t ring_phase(int pos) {
-  return (static_cast<unsigned>(pos) / kStages) & 1u;
+  return (static_cast<unsigned>(pos) / R) & 1u;
 }
 
 // Block-sparse tile list, built by warp 0 with ballots: the tiles t in
@@ -179,7 +226,11 @@ __device__ __forceinline__ bool bwd_init(BwdBars* bars, int warp, uint32_t cols)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->str_full[s], 1);
       mbar_init(&bars->str_empty[s], 1);
+      mbar_init(&bars->str_full_hi[s], 1);
+      mbar_init(&bars->str_empty_hi[s], 1);
     }
+    mbar_init(&bars->s_full_1, 1);
+    mbar_init(&bars->p_ready_1, kComputeThreads);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, kComputeThreads);
@@ -252,20 +303,21 @@ __device__ __forceinline__ bool bwd_producer_item(uint8_t* smem, BwdBars* bars,
   };
   if (t == 0) load_res();
   for (int n = 0; n < ntiles; ++n) {
-    const int s = ring_slot(sb + n);
-    const uint32_t ph = ring_phase(sb + n);
-    bool ok = mbar_wait(&bars->str_empty[s], ph ^ 1, &bars->abort_flag, &g_bwd_error, 0x101);
+    const int s = ring_slot<L::kRing>(sb + n);
+    const uint32_t ph = ring_phase<L::kRing>(sb + n);
+    bool ok = mbar_wait(str_empty_bar<L::kRing>(bars, s), ph ^ 1, &bars->abort_flag, &g_bwd_error,
+                        0x101);
     if (!__all_sync(0xffffffffu, ok)) return false;
     const int row0 = (list ? static_cast<int>(list[n]) : first_tile + n) * 128;
     // the tiles first, then (while they are in flight) the staged vectors; the
     // stage's one arrival comes last, after both
     if (lane == 0) {
-      mbar_expect_tx(&bars->str_full[s], 2 * L::kTileBytes);
+      mbar_expect_tx(str_full_bar<L::kRing>(bars, s), 2 * L::kTileBytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, &bars->str_full[s],
+        tma_load_3d(smem + L::kStr0 + s * L::kTileBytes + c * 16384, s0, str_full_bar<L::kRing>(bars, s),
                     c * 64, row0, bh);
-        tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, &bars->str_full[s],
+        tma_load_3d(smem + L::kStr1 + s * L::kTileBytes + c * 16384, s1, str_full_bar<L::kRing>(bars, s),
                     c * 64, row0, bh);
       }
     }
@@ -280,7 +332,7 @@ __device__ __forceinline__ bool bwd_producer_item(uint8_t* smem, BwdBars* bars,
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->str_full[s]);
+    if (lane == 0) mbar_arrive(str_full_bar<L::kRing>(bars, s));
     __syncwarp();
     if (n == 0 && t > 0) {
       ok = mbar_wait(&bars->res_empty, (t - 1) & 1, &bars->abort_flag, &g_bwd_error, 0x102);
@@ -557,16 +609,98 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(&bars->res_empty);  // K, V free once the products above complete
         return ok;
       };
+      // d = 64 (two score buffers, four-stage ring): the next step's scores
+      // go first, into the other score buffer (the P there was read by the dV
+      // of the step before, issued earlier), so that they are ready when the
+      // compute warps finish a step; the ring has their tiles in well ahead.
+      // Otherwise as mma_item.
+      auto slot4 = [](int pos) { return ring_slot<L::kRing>(pos); };
+      auto phase4 = [](int pos) { return ring_phase<L::kRing>(pos); };
+      auto sQ4 = [&](int pos) { return smem_u32(smem + L::kStr0 + slot4(pos) * L::kTileBytes); };
+      auto sdO4 = [&](int pos) { return smem_u32(smem + L::kStr1 + slot4(pos) * L::kTileBytes); };
+      auto mma_item_ds = [&](const int item, const int t, const int sb, const int nb) -> bool {
+        const int n_iters = item_iters(item);
+        if (n_iters == 0) return true;
+        auto issue_s4 = [&](int pos, uint32_t col) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + col, kmajor_desc(sK, kk), kmajor_desc(sQ4(pos), kk), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        };
+        auto issue_dp4 = [&](int pos) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + L::kDPCol, kmajor_desc(sV, kk), kmajor_desc(sdO4(pos), kk), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        };
+        bool ok = mbar_wait(&bars->res_full, t & 1, &bars->abort_flag, &g_bwd_error, 0x201) &&
+                  mbar_wait(str_full_bar<L::kRing>(bars, slot4(sb)), phase4(sb), &bars->abort_flag,
+                            &g_bwd_error, 0x202);
+        if (!ok) return false;
+        tc_fence_after_sync();
+        issue_s4(sb, L::s_col(nb));
+        umma_commit(s_full_bar<true>(bars, nb));
+        issue_dp4(sb);
+        umma_commit(&bars->dp_full);
+        for (int n = 0; n < n_iters; ++n) {
+          const int pos = sb + n;
+          const bool more = n + 1 < n_iters;
+          if (more) {
+            if (!mbar_wait(str_full_bar<L::kRing>(bars, slot4(pos + 1)), phase4(pos + 1),
+                           &bars->abort_flag, &g_bwd_error, 0x208)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_s4(pos + 1, L::s_col(nb + n + 1));
+            umma_commit(s_full_bar<true>(bars, nb + n + 1));
+          }
+          if (!mbar_wait(p_ready_bar<true>(bars, nb + n), s_parity<true>(nb + n), &bars->abort_flag,
+                         &g_bwd_error, 0x203) ||
+              (n == 0 && t > 0 &&
+               !mbar_wait(&bars->acc_free, (t - 1) & 1, &bars->abort_flag, &g_bwd_error, 0x206))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + L::kAcc0, tmem + L::s_col(nb + n) + packed_a_col(kk),
+                    mnmajor_desc(sdO4(pos), kk), idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          if (!mbar_test_wait(&bars->ds_ready, (nb + n) & 1) &&
+              !mbar_wait(&bars->ds_ready, (nb + n) & 1, &bars->abort_flag, &g_bwd_error, 0x204)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + L::kAcc1, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sQ4(pos), kk),
+                    idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(str_empty_bar<L::kRing>(bars, slot4(pos)));
+          if (more) {
+            issue_dp4(pos + 1);
+            umma_commit(&bars->dp_full);
+          }
+        }
+        if (ok) umma_commit(&bars->acc_done);
+        umma_commit(&bars->res_empty);
+        return ok;
+      };
       if (PERSIST) {
         auto mwait = [&](uint64_t* bar, uint32_t par) {
           return mbar_wait(bar, par, &bars->abort_flag, &g_bwd_error, 0x207);
         };
         for (int t = 0, sb = 0, nb = 0;; ++t) {
           const int item = consumer_item(t, mwait);
-          if (item < 0 || !mma_item(item, t, sb, nb)) break;
+          if (item < 0 ||
+              !(L::kDoubleS ? mma_item_ds(item, t, sb, nb) : mma_item(item, t, sb, nb)))
+            break;
           sb += item_iters(item);
           nb += item_iters(item);
         }
+      } else if (L::kDoubleS) {
+        mma_item_ds(static_cast<int>(blockIdx.x), 0, 0, 0);
       } else {
         mma_item(static_cast<int>(blockIdx.x), 0, 0, 0);
       }
@@ -596,7 +730,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int it = SPARSE ? static_cast<int>(list[n]) : item_first(item) + n;
       const int q0 = it * 128;
       // lse * log2(e) and D of this query tile, staged with the tiles
-      const float* lse2_s = vec + ring_slot(nb + n) * 256;
+      const float* lse2_s = vec + ring_slot<L::kRing>(nb + n) * 256;
       const float* D_s = lse2_s + 128;
       // dropout keep bits of this key row for query rows q0 + col0 + c (bit c
       // of kb[c / 32]), drawn before the scores are waited for
@@ -607,14 +741,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           kb[w] = keep_word_t(drop, pcol, static_cast<uint32_t>(q0) + col0 + 32u * w, lane);
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
-      if (!bwd_warp_wait(&bars->s_full, (nb + n) & 1, bars, 0x301)) {
+      if (!bwd_warp_wait(s_full_bar<L::kDoubleS>(bars, nb + n), s_parity<L::kDoubleS>(nb + n),
+                         bars, 0x301)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       // P^T for this key row and query columns [col0, col0+64)
       uint32_t pr[64];
-      tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
+      tmem_ld64(tmem + lane_off + L::s_col(nb + n) + col0, pr);
       // only the diagonal tile needs the causal mask (query rows past N have
       // lse = +inf staged, so their P is 0 without one); the test is uniform
       // across the warp
@@ -657,11 +792,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[c] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st32(tmem + lane_off + L::kSCol + col0, pk);
+        tmem_st32(tmem + lane_off + L::s_col(nb + n) + col0, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->p_ready);
+      mbar_arrive(p_ready_bar<L::kDoubleS>(bars, nb + n));
       if (!bwd_warp_wait(&bars->dp_full, (nb + n) & 1, bars, 0x304)) {
         ok = false;
         break;
@@ -942,15 +1077,93 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(&bars->res_empty);  // Q, dO free once the products above complete
         return ok;
       };
+      // d = 64 (two score buffers, four-stage ring): the next step's scores
+      // go first, as in the dK/dV kernel.  Otherwise as mma_item.
+      auto slot4 = [](int pos) { return ring_slot<L::kRing>(pos); };
+      auto phase4 = [](int pos) { return ring_phase<L::kRing>(pos); };
+      auto sK4 = [&](int pos) { return smem_u32(smem + L::kStr0 + slot4(pos) * L::kTileBytes); };
+      auto sV4 = [&](int pos) { return smem_u32(smem + L::kStr1 + slot4(pos) * L::kTileBytes); };
+      auto mma_item_ds = [&](const int item, const int t, const int sb) -> bool {
+        const int n_iters = item_iters(item);
+        if (n_iters == 0) return true;
+        auto issue_s4 = [&](int pos, uint32_t col) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + col, kmajor_desc(sQ, kk), kmajor_desc(sK4(pos), kk), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        };
+        auto issue_dp4 = [&](int pos) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + L::kDPCol, kmajor_desc(sdO, kk), kmajor_desc(sV4(pos), kk), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        };
+        bool ok = mbar_wait(&bars->res_full, t & 1, &bars->abort_flag, &g_bwd_error, 0x211) &&
+                  mbar_wait(str_full_bar<L::kRing>(bars, slot4(sb)), phase4(sb), &bars->abort_flag,
+                            &g_bwd_error, 0x212);
+        if (!ok) return false;
+        tc_fence_after_sync();
+        issue_s4(sb, L::s_col(sb));
+        umma_commit(s_full_bar<true>(bars, sb));
+        issue_dp4(sb);
+        umma_commit(&bars->dp_full);
+        for (int n = 0; n < n_iters; ++n) {
+          const int pos = sb + n;
+          const bool more = n + 1 < n_iters;
+          if (more) {
+            if (!mbar_wait(str_full_bar<L::kRing>(bars, slot4(pos + 1)), phase4(pos + 1),
+                           &bars->abort_flag, &g_bwd_error, 0x218)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_s4(pos + 1, L::s_col(pos + 1));
+            umma_commit(s_full_bar<true>(bars, pos + 1));
+          }
+          if (!mbar_wait(p_ready_bar<true>(bars, pos), s_parity<true>(pos), &bars->abort_flag,
+                         &g_bwd_error, 0x214) ||
+              (n == 0 && t > 0 &&
+               !mbar_wait(&bars->acc_free, (t - 1) & 1, &bars->abort_flag, &g_bwd_error, 0x216))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + kB, tmem + L::s_col(pos) + packed_a_col(kk), mnmajor_desc(sK4(pos), kk),
+                    idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          if (!mbar_test_wait(&bars->ds_ready, pos & 1) &&
+              !mbar_wait(&bars->ds_ready, pos & 1, &bars->abort_flag, &g_bwd_error, 0x213)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + kDQ, tmem + L::kDPCol + packed_a_col(kk), mnmajor_desc(sK4(pos), kk),
+                    idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(str_empty_bar<L::kRing>(bars, slot4(pos)));
+          if (more) {
+            issue_dp4(pos + 1);
+            umma_commit(&bars->dp_full);
+          }
+        }
+        if (ok) umma_commit(&bars->acc_done);
+        umma_commit(&bars->res_empty);
+        return ok;
+      };
       if (PERSIST) {
         auto mwait = [&](uint64_t* bar, uint32_t par) {
           return mbar_wait(bar, par, &bars->abort_flag, &g_bwd_error, 0x217);
         };
         for (int t = 0, sb = 0;; ++t) {
           const int item = consumer_item(t, mwait);
-          if (item < 0 || !mma_item(item, t, sb)) break;
+          if (item < 0 || !(L::kDoubleS ? mma_item_ds(item, t, sb) : mma_item(item, t, sb)))
+            break;
           sb += item_iters(item);
         }
+      } else if (L::kDoubleS) {
+        mma_item_ds(static_cast<int>(blockIdx.x), 0, 0);
       } else {
         mma_item(static_cast<int>(blockIdx.x), 0, 0);
       }
@@ -990,13 +1203,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           kb[u >> 2] |= keep_byte_row(drop, prow, jg0 + u) << (8 * (u & 3));
         reg_pin(kb);  // drawn here, before the wait, not next to their use
       }
-      if (!bwd_warp_wait(&bars->s_full, (nb + n) & 1, bars, 0x311)) {
+      if (!bwd_warp_wait(s_full_bar<L::kDoubleS>(bars, nb + n), s_parity<L::kDoubleS>(nb + n),
+                         bars, 0x311)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       uint32_t pr[64];
-      tmem_ld64(tmem + lane_off + L::kSCol + col0, pr);
+      tmem_ld64(tmem + lane_off + L::s_col(nb + n) + col0, pr);
       const int kv0 = kt_of(n) * 128;
       // only the diagonal tile (causal) and a ragged last tile need a mask:
       // the test is uniform across the warp, so other tiles skip it
@@ -1031,11 +1245,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c)
           pk[c] = pack_bf16x2(__uint_as_float(pr[2 * c]), __uint_as_float(pr[2 * c + 1]));
-        tmem_st32(tmem + lane_off + L::kSCol + col0, pk);
+        tmem_st32(tmem + lane_off + L::s_col(nb + n) + col0, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->p_ready);
+      mbar_arrive(p_ready_bar<L::kDoubleS>(bars, nb + n));
       if (!bwd_warp_wait(&bars->dp_full, (nb + n) & 1, bars, 0x314)) {
         ok = false;
         break;
