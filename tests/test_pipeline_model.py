@@ -1,0 +1,298 @@
+"""A host model of the dK/dV kernel's barrier protocol, run under random schedules.
+
+The kernel's roles (TMA producer, MMA issuer, compute warps) synchronise through
+mbarriers whose waits test a phase *parity*: a wait for phase k returns once
+phase k has completed, but if the barrier has meanwhile completed phase k + 1
+as well, the parity matches the incomplete phase k + 2 and the waiter hangs
+(the kernel's bounded wait then reports a timeout).  The order of products and
+barriers must therefore never let a barrier run two phases ahead of one of its
+waiters.  At d = 64 the kernel keeps two score buffers and issues the next
+step's score product before the current step's P is consumed; each buffer has
+its own "scores ready" and "P ready" barrier for that reason.
+
+This model replays the protocol of csrc/fa_bwd.cu (the dK/dV kernel; the dQ
+kernel's is the same with other operands) with true parity semantics: the
+tensor core completes products in issue order, a commit's arrival fires when
+the products issued before it have completed, tile loads land in any order,
+and every role advances at random.  The compute side is two warps that each
+own half of every score and dP buffer, arrive on the counting barriers on
+their own and may drift a step apart.  It checks over many schedules,
+persistent items included, that every run ends (no wait hangs), that every
+product and every warp reads the data its step needs (the scores, P and dS of
+its own step, not of another), and that no product overwrites data a later
+reader still needs.
+"""
+import random
+
+import pytest
+
+
+class Barrier:
+    def __init__(self, count):
+        self.count = count
+        self.pending = 0
+        self.phases = 0  # completed phases
+
+    def arrive(self):
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending = 0
+            self.phases += 1
+
+    def done(self, parity):
+        # mbarrier try_wait.parity: true when the current phase's parity differs
+        return (self.phases & 1) != parity
+
+
+class Model:
+    def __init__(self, rng, items, ring, double_s):
+        self.rng = rng
+        self.items = items  # steps per item, one persistent CTA
+        self.R = ring
+        self.ds = double_s
+        B = Barrier
+        self.str_full = [B(1) for _ in range(ring)]
+        self.str_empty = [B(1) for _ in range(ring)]
+        W = self.W = 2  # compute warps, each owning half of every buffer
+        self.s_full = [B(1), B(1)]
+        self.p_ready = [B(W), B(W)]
+        self.dp_full, self.ds_ready = B(1), B(W)
+        self.acc_done, self.acc_free, self.res_empty, self.res_full = B(1), B(W), B(1), B(1)
+        self.queue = []  # tensor core: in-order products and commits
+        self.loads = []  # tile loads in flight (complete in any order)
+        self.slot_tile = [None] * ring  # step whose tiles a ring slot holds
+        # [buffer][warp half]: ("S" or "P", step); [warp half]: ("dP" or "dS", step)
+        self.sbuf = [[None] * W, [None] * W]
+        self.dpbuf = [None] * W
+        self.sbuf_consumed = [[True] * W, [True] * W]
+        self.dp_consumed = [True] * W
+        self.errors = []
+
+    # --- helpers mirroring the kernel's
+    def buf(self, g):
+        return (g & 1) if self.ds else 0
+
+    def spar(self, g):
+        return ((g >> 1) & 1) if self.ds else (g & 1)
+
+    def slot(self, pos):
+        return pos % self.R
+
+    def phase(self, pos):
+        return (pos // self.R) & 1
+
+    # --- the tensor core executes the head of its queue
+    def tensor_step(self):
+        kind, arg = self.queue.pop(0)
+        if kind == "commit":
+            arg.arrive()
+            return
+        op, g = kind, arg
+        b = self.buf(g)
+        for w in range(self.W):
+            if op == "S":
+                if self.sbuf[b][w] is not None and self.sbuf[b][w][0] == "P" \
+                        and not self.sbuf_consumed[b][w]:
+                    self.errors.append(f"S_{g} overwrote P_{self.sbuf[b][w][1]} before dV read it")
+                self.sbuf[b][w] = ("S", g)
+                self.sbuf_consumed[b][w] = False
+            elif op == "dP":
+                if self.dpbuf[w] is not None and self.dpbuf[w][0] == "dS" \
+                        and not self.dp_consumed[w]:
+                    self.errors.append(f"dP_{g} overwrote dS_{self.dpbuf[w][1]} before dK read it")
+                self.dpbuf[w] = ("dP", g)
+                self.dp_consumed[w] = False
+            elif op == "dV":
+                if self.sbuf[b][w] != ("P", g):
+                    self.errors.append(f"dV_{g} read {self.sbuf[b][w]}")
+                self.sbuf_consumed[b][w] = True
+            elif op == "dK":
+                if self.dpbuf[w] != ("dS", g):
+                    self.errors.append(f"dK_{g} read {self.dpbuf[w]}")
+                self.dp_consumed[w] = True
+        if op in ("S", "dK") and self.slot_tile[self.slot(g)] != g:
+            self.errors.append(f"{op}_{g} read the tiles of step {self.slot_tile[self.slot(g)]}")
+
+    # --- roles as generators: each `yield cond` blocks until cond() holds
+    def producer(self):
+        sb = 0
+        for t, n_steps in enumerate(self.items):
+            for n in range(n_steps):
+                pos = sb + n
+                s = self.slot(pos)
+                bar = self.str_empty[s]
+                yield lambda b=bar, p=self.phase(pos) ^ 1: b.done(p)
+                self.loads.append((s, pos))
+                if n == 0 and t > 0:
+                    yield lambda p=(t - 1) & 1: self.res_empty.done(p)
+                if n == 0:
+                    self.res_full.arrive()
+            sb += n_steps
+
+    def mma(self):
+        sb = 0
+        for t, n_steps in enumerate(self.items):
+            yield lambda p=t & 1: self.res_full.done(p)
+            yield lambda s=self.slot(sb), p=self.phase(sb): self.str_full[s].done(p)
+            self.queue += [("S", sb), ("commit", self.s_full[self.buf(sb)]), ("dP", sb),
+                           ("commit", self.dp_full)]
+            for n in range(n_steps):
+                g = sb + n
+                more = n + 1 < n_steps
+                if self.ds and more:  # the next step's scores first
+                    yield lambda s=self.slot(g + 1), p=self.phase(g + 1): self.str_full[s].done(p)
+                    self.queue += [("S", g + 1), ("commit", self.s_full[self.buf(g + 1)])]
+                yield lambda b=self.buf(g), p=self.spar(g): self.p_ready[b].done(p)
+                if n == 0 and t > 0:
+                    yield lambda p=(t - 1) & 1: self.acc_free.done(p)
+                self.queue.append(("dV", g))
+                if not self.ds and more:
+                    yield lambda s=self.slot(g + 1), p=self.phase(g + 1): self.str_full[s].done(p)
+                    self.queue += [("S", g + 1), ("commit", self.s_full[0])]
+                yield lambda p=g & 1: self.ds_ready.done(p)
+                self.queue += [("dK", g), ("commit", self.str_empty[self.slot(g)])]
+                if more:
+                    self.queue += [("dP", g + 1), ("commit", self.dp_full)]
+            self.queue += [("commit", self.acc_done), ("commit", self.res_empty)]
+            sb += n_steps
+
+    def compute(self, w):
+        nb = 0
+        for t, n_steps in enumerate(self.items):
+            for n in range(n_steps):
+                g = nb + n
+                b = self.buf(g)
+                yield lambda b=b, p=self.spar(g): self.s_full[b].done(p)
+                if self.sbuf[b][w] != ("S", g):
+                    self.errors.append(f"warp {w} step {g} read scores {self.sbuf[b][w]}")
+                yield None  # the exponentials take a while
+                self.sbuf[b][w] = ("P", g)
+                self.sbuf_consumed[b][w] = False
+                self.p_ready[b].arrive()
+                yield lambda p=g & 1: self.dp_full.done(p)
+                if self.dpbuf[w] != ("dP", g):
+                    self.errors.append(f"warp {w} step {g} read dP {self.dpbuf[w]}")
+                yield None
+                self.dpbuf[w] = ("dS", g)
+                self.dp_consumed[w] = False
+                self.ds_ready.arrive()
+            yield lambda p=t & 1: self.acc_done.done(p)
+            yield None  # the epilogue
+            self.acc_free.arrive()
+            nb += n_steps
+
+    def run(self):
+        roles = {"producer": self.producer(), "mma": self.mma()}
+        for w in range(self.W):
+            roles[f"compute{w}"] = self.compute(w)
+        waiting = {name: None for name in roles}
+        finished = set()
+        for _ in range(200000):
+            enabled = []
+            for name, gen in roles.items():
+                if name in finished:
+                    continue
+                cond = waiting[name]
+                if cond is None or cond():
+                    enabled.append(name)
+            if self.queue:
+                enabled.append("tensor")
+            if self.loads:
+                enabled.append("tma")
+            if not enabled:
+                break
+            pick = self.rng.choice(enabled)
+            if pick == "tensor":
+                self.tensor_step()
+            elif pick == "tma":
+                s, pos = self.loads.pop(self.rng.randrange(len(self.loads)))
+                self.slot_tile[s] = pos
+                self.str_full[s].arrive()
+            else:
+                try:
+                    waiting[pick] = next(roles[pick])
+                except StopIteration:
+                    finished.add(pick)
+                    waiting[pick] = None
+        return finished == set(roles) and not self.queue and not self.loads
+
+
+@pytest.mark.parametrize("double_s,ring", [(False, 2), (True, 4)], ids=["d128", "d64"])
+def test_protocol_never_hangs_and_reads_its_own_step(double_s, ring):
+    rng = random.Random(20261203 + ring)
+    for trial in range(300):
+        items = [rng.randint(1, 6) for _ in range(rng.randint(1, 4))]
+        m = Model(rng, items, ring, double_s)
+        assert m.run(), f"schedule {trial} (items {items}) hung"
+        assert not m.errors, f"schedule {trial} (items {items}): {m.errors[:3]}"
+
+
+def test_one_score_barrier_would_alias_at_d64():
+    """The reason each score buffer has its own barriers: with one shared
+    "scores ready" / "P ready" barrier and the next scores issued first, some
+    schedule lets a barrier run two phases ahead, and a wait hangs."""
+
+    class SharedBarriers(Model):
+        def buf(self, g):  # the buffer still alternates ...
+            return g & 1
+
+        def spar(self, g):  # ... but every step waits on barrier [0]
+            return g & 1
+
+        def mma(self):
+            self.s_full[1] = self.s_full[0]
+            self.p_ready[1] = self.p_ready[0]
+            yield from super().mma()
+
+    rng = random.Random(7)
+    hung = 0
+    for _ in range(300):
+        items = [rng.randint(2, 6) for _ in range(rng.randint(1, 3))]
+        if not SharedBarriers(rng, items, 4, True).run():
+            hung += 1
+    assert hung > 0
+
+
+@pytest.mark.parametrize("double_s,ring", [(False, 2), (True, 4)], ids=["d128", "d64"])
+def test_model_sees_a_load_that_skips_the_empty_wait(double_s, ring):
+    """The model itself is sensitive: a producer that reloads a ring slot
+    without waiting for the products that read it is caught."""
+
+    class EarlyLoad(Model):
+        def producer(self):
+            sb = 0
+            for t, n_steps in enumerate(self.items):
+                for n in range(n_steps):
+                    pos = sb + n
+                    self.loads.append((self.slot(pos), pos))
+                    if n == 0 and t > 0:
+                        yield lambda p=(t - 1) & 1: self.res_empty.done(p)
+                    if n == 0:
+                        self.res_full.arrive()
+                    yield None
+                sb += n_steps
+
+    rng = random.Random(3)
+    bad = 0
+    for _ in range(100):
+        items = [rng.randint(2, 6) for _ in range(rng.randint(1, 4))]
+        m = EarlyLoad(rng, items, ring, double_s)
+        bad += (not m.run()) or bool(m.errors)
+    assert bad > 0
+
+
+def test_model_sees_one_score_buffer_with_early_scores():
+    """Issuing the next step's scores first into the same buffer overwrites a
+    P that dV has not read; the model reports it."""
+
+    class OneBuffer(Model):
+        def buf(self, g):
+            return 0
+
+    rng = random.Random(5)
+    bad = 0
+    for _ in range(100):
+        items = [rng.randint(2, 6) for _ in range(rng.randint(1, 4))]
+        m = OneBuffer(rng, items, 4, True)
+        bad += (not m.run()) or bool(m.errors)
+    assert bad > 0
