@@ -1,4 +1,4 @@
-"""A host model of the dK/dV kernel's barrier protocol, run under random schedules.
+"""Host models of the attention kernels' barrier protocols, run under random schedules.
 
 The kernel's roles (TMA producer, MMA issuer, compute warps) synchronise through
 mbarriers whose waits test a phase *parity*: a wait for phase k returns once
@@ -10,8 +10,9 @@ waiters.  At d = 64 the kernel keeps two score buffers and issues the next
 step's score product before the current step's P is consumed; each buffer has
 its own "scores ready" and "P ready" barrier for that reason.
 
-This model replays the protocol of csrc/fa_bwd.cu (the dK/dV kernel; the dQ
-kernel's is the same with other operands) with true parity semantics: the
+`Model` replays the protocol of csrc/fa_bwd.cu (the dK/dV kernel; the dQ
+kernel's is the same with B = P K in place of dV and dQ~ in place of dK) and
+`FwdModel` that of csrc/fa_fwd.cu, both with true parity semantics: the
 tensor core completes products in issue order, a commit's arrival fires when
 the products issued before it have completed, tile loads land in any order,
 and every role advances at random.  The compute side is two warps that each
@@ -20,7 +21,10 @@ their own and may drift a step apart.  It checks over many schedules,
 persistent items included, that every run ends (no wait hangs), that every
 product and every warp reads the data its step needs (the scores, P and dS of
 its own step, not of another), and that no product overwrites data a later
-reader still needs.
+reader still needs.  The forward's issuer sends each key tile's products in
+two bursts and tests (without blocking) whether the second group's P is ready
+before it commits the first group's scores; its model takes both branches of
+that test, and checks the item ring the TMA warp publishes claimed items in.
 """
 import random
 
@@ -294,5 +298,293 @@ def test_model_sees_one_score_buffer_with_early_scores():
     for _ in range(100):
         items = [rng.randint(2, 6) for _ in range(rng.randint(1, 4))]
         m = OneBuffer(rng, items, 4, True)
+        bad += (not m.run()) or bool(m.errors)
+    assert bad > 0
+
+
+class FwdModel:
+    """The forward kernel: one item is a pair of query tiles (groups 0 and 1,
+    n0 and n1 key tiles, n0 <= n1), Q resident, K and V streamed through a
+    two-stage ring, each group's scores and P in one tensor-memory buffer and
+    its O accumulator in another; claimed items reach the other roles through
+    a four-entry ring."""
+
+    RING_ITEMS = 4
+
+    def __init__(self, rng, items, warps=2):
+        self.rng = rng
+        self.items = items  # (n0, n1) per item of one persistent CTA
+        self.W = W = warps  # warps per softmax group, each owning part of the rows
+        B = Barrier
+        self.q_full, self.q_empty = B(1), B(1)
+        self.k_full, self.k_empty = [B(1), B(1)], [B(1), B(1)]
+        self.v_full, self.v_empty = [B(1), B(1)], [B(1), B(1)]
+        self.s_full = [B(1), B(1)]
+        self.p_ready = [B(W), B(W)]
+        self.pv_done = [B(1), B(1)]
+        self.o_free = [B(W), B(W)]
+        self.item_full = [B(1) for _ in range(self.RING_ITEMS)]
+        self.item_ring = [None] * self.RING_ITEMS
+        self.item_readers = [set() for _ in range(self.RING_ITEMS)]
+        self.n_readers = 1 + 2 * W  # the issuer and every softmax warp
+        self.queue, self.loads = [], []
+        self.q_tile = None
+        self.k_tile, self.v_tile = [None, None], [None, None]
+        # per group and warp: ("S" | "P", item, tile) and (item, PV products in O)
+        self.sbuf = [[None] * W for _ in range(2)]
+        self.p_read = [[True] * W for _ in range(2)]
+        self.obuf = [[None] * W for _ in range(2)]
+        self.o_read = [[True] * W for _ in range(2)]
+        self.errors = []
+
+    @staticmethod
+    def slot(pos):
+        return pos % 2
+
+    @staticmethod
+    def phase(pos):
+        return (pos // 2) & 1
+
+    def tensor_step(self):
+        kind, *arg = self.queue.pop(0)
+        if kind == "commit":
+            arg[0].arrive()
+            return
+        g, pos, t, j = arg[:4]
+        if kind == "S":
+            if self.q_tile != t:
+                self.errors.append(f"S{g} of item {t} read the Q of item {self.q_tile}")
+            if self.k_tile[self.slot(pos)] != pos:
+                self.errors.append(f"S{g} at {pos} read the K tile {self.k_tile[self.slot(pos)]}")
+            for w in range(self.W):
+                if not self.p_read[g][w]:
+                    self.errors.append(f"S{g}({t},{j}) overwrote a P before P V read it")
+                self.sbuf[g][w] = ("S", t, j)
+        else:  # "PV"
+            first = arg[4]
+            if self.v_tile[self.slot(pos)] != pos:
+                self.errors.append(f"PV{g} at {pos} read the V tile {self.v_tile[self.slot(pos)]}")
+            for w in range(self.W):
+                if self.sbuf[g][w] != ("P", t, j):
+                    self.errors.append(f"PV{g}({t},{j}) read {self.sbuf[g][w]}")
+                self.p_read[g][w] = True
+                if first:
+                    if not self.o_read[g][w]:
+                        self.errors.append(f"PV{g} of item {t} overwrote an O not yet stored")
+                    self.obuf[g][w] = (t, 1)
+                    self.o_read[g][w] = False
+                elif self.obuf[g][w] != (t, j):
+                    self.errors.append(f"PV{g}({t},{j}) accumulated into {self.obuf[g][w]}")
+                else:
+                    self.obuf[g][w] = (t, j + 1)
+
+    def publish(self, t, item):
+        r = t % self.RING_ITEMS
+        if t >= self.RING_ITEMS and len(self.item_readers[r]) < self.n_readers:
+            self.errors.append(f"item ring entry {r} overwritten before every role read it")
+        self.item_ring[r] = item
+        self.item_readers[r] = set()
+        self.item_full[r].arrive()
+
+    def claim(self, t, who):
+        r = t % self.RING_ITEMS
+        yield lambda: self.item_full[r].done((t // self.RING_ITEMS) & 1)
+        self.item_readers[r].add(who)
+        return self.item_ring[r]
+
+    def producer(self):
+        kvb = 0
+        for t, item in enumerate(self.items + [None]):
+            self.publish(t, item)
+            if item is None:
+                return
+            n0, n1 = item
+            if t == 0 and n1 > 0:
+                self.loads.append(("Q", t))
+            for j in range(n1):
+                pos = kvb + j
+                s, ph = self.slot(pos), self.phase(pos)
+                yield lambda s=s, p=ph ^ 1: self.k_empty[s].done(p)
+                self.loads.append(("K", pos))
+                if j == 0 and t > 0:
+                    yield lambda p=(t - 1) & 1: self.q_empty.done(p)
+                    self.loads.append(("Q", t))
+                yield lambda s=s, p=ph ^ 1: self.v_empty[s].done(p)
+                self.loads.append(("V", pos))
+            kvb += n1
+
+    def land(self, load):
+        kind, x = load
+        if kind == "Q":
+            self.q_tile = x
+            self.q_full.arrive()
+        elif kind == "K":
+            self.k_tile[self.slot(x)] = x
+            self.k_full[self.slot(x)].arrive()
+        else:
+            self.v_tile[self.slot(x)] = x
+            self.v_full[self.slot(x)].arrive()
+
+    def mma(self):
+        kvb = base0 = base1 = 0
+        for t in range(len(self.items) + 1):
+            item = yield from self.claim(t, "mma")
+            if item is None:
+                return
+            n0, n1 = item
+            if n1 == 0:  # a block-sparse item without key tiles (a CTA's only item)
+                continue
+            yield lambda p=t & 1: self.q_full.done(p)
+            yield lambda s=self.slot(kvb), p=self.phase(kvb): self.k_full[s].done(p)
+            self.queue += [("S", 0, kvb, t, 0), ("commit", self.s_full[0]),
+                           ("S", 1, kvb, t, 0), ("commit", self.s_full[1]),
+                           ("commit", self.k_empty[self.slot(kvb)])]
+            for j in range(n1):
+                pos = kvb + j
+                s, ph = self.slot(pos), self.phase(pos)
+                sn, phn = self.slot(pos + 1), self.phase(pos + 1)
+                pre1 = False
+                if j < n0:
+                    yield lambda p=(base0 + j) & 1: self.p_ready[0].done(p)
+                    yield lambda: self.v_full[s].done(ph)
+                    if j == 0 and t > 0:
+                        yield lambda p=(t - 1) & 1: self.o_free[0].done(p)
+                    if j + 1 < n1:
+                        yield lambda: self.k_full[sn].done(phn)
+                    self.queue += [("PV", 0, pos, t, j, j == 0), ("commit", self.pv_done[0])]
+                    if j + 1 < n0:
+                        self.queue.append(("S", 0, pos + 1, t, j + 1))
+                    yield None  # the issue takes a while; the others move meanwhile
+                    pre1 = self.p_ready[1].done((base1 + j) & 1) and (
+                        j > 0 or t == 0 or self.o_free[1].done((t - 1) & 1))
+                    if j + 1 < n0:
+                        self.queue.append(("commit", self.s_full[0]))
+                if not pre1:
+                    yield lambda p=(base1 + j) & 1: self.p_ready[1].done(p)
+                    if j >= n0:
+                        yield lambda: self.v_full[s].done(ph)
+                    if j == 0 and t > 0:
+                        yield lambda p=(t - 1) & 1: self.o_free[1].done(p)
+                    if j >= n0 and j + 1 < n1:
+                        yield lambda: self.k_full[sn].done(phn)
+                self.queue += [("PV", 1, pos, t, j, j == 0), ("commit", self.v_empty[s])]
+                if j + 1 < n1:
+                    self.queue.append(("S", 1, pos + 1, t, j + 1))
+                self.queue.append(("commit", self.pv_done[1]))
+                if j + 1 < n1:
+                    self.queue += [("commit", self.s_full[1]), ("commit", self.k_empty[sn])]
+            self.queue.append(("commit", self.q_empty))
+            kvb += n1
+            base0 += n0
+            base1 += n1
+
+    def softmax(self, g, w):
+        tb = 0
+        for t in range(len(self.items) + 1):
+            item = yield from self.claim(t, ("softmax", g, w))
+            if item is None:
+                return
+            nkv = item[g]
+            for j in range(nkv):
+                yield lambda p=(tb + j) & 1: self.s_full[g].done(p)
+                if self.sbuf[g][w] != ("S", t, j):
+                    self.errors.append(f"softmax {g}.{w} at ({t},{j}) read {self.sbuf[g][w]}")
+                yield None  # the exponentials
+                if j > 0 and self.obuf[g][w] != (t, j):  # the lazy rescale of O
+                    self.errors.append(f"softmax {g}.{w} rescaled O {self.obuf[g][w]} at ({t},{j})")
+                yield None
+                if j > 0 and self.obuf[g][w] != (t, j):
+                    self.errors.append(f"O {g}.{w} changed under the rescale at ({t},{j})")
+                self.sbuf[g][w] = ("P", t, j)
+                self.p_read[g][w] = False
+                self.p_ready[g].arrive()
+            if nkv > 0:
+                yield lambda p=(tb + nkv - 1) & 1: self.pv_done[g].done(p)
+                if self.obuf[g][w] != (t, nkv):
+                    self.errors.append(f"epilogue {g}.{w} of item {t} read O {self.obuf[g][w]}")
+                yield None  # the stores
+                if self.obuf[g][w] != (t, nkv):
+                    self.errors.append(f"O {g}.{w} changed under the epilogue of item {t}")
+                self.o_read[g][w] = True
+            self.o_free[g].arrive()
+            tb += nkv
+
+    def run(self):
+        roles = {"producer": self.producer(), "mma": self.mma()}
+        for g in range(2):
+            for w in range(self.W):
+                roles[("softmax", g, w)] = self.softmax(g, w)
+        waiting = {name: None for name in roles}
+        finished = set()
+        for _ in range(400000):
+            enabled = [n for n in roles if n not in finished
+                       and (waiting[n] is None or waiting[n]())]
+            if self.queue:
+                enabled.append("tensor")
+            if self.loads:
+                enabled.append("tma")
+            if not enabled:
+                break
+            pick = self.rng.choice(enabled)
+            if pick == "tensor":
+                self.tensor_step()
+            elif pick == "tma":
+                self.land(self.loads.pop(self.rng.randrange(len(self.loads))))
+            else:
+                try:
+                    waiting[pick] = next(roles[pick])
+                except StopIteration:
+                    finished.add(pick)
+                    waiting[pick] = None
+        return finished == set(roles) and not self.queue and not self.loads
+
+
+def fwd_items(rng, causal):
+    out = []
+    for _ in range(rng.randint(1, 5)):
+        n0 = rng.randint(1, 6)
+        out.append((n0, n0 + (rng.random() < 0.7)) if causal else (n0, n0))
+    return out
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_forward_protocol_never_hangs_and_reads_its_own_tile(causal):
+    rng = random.Random(20261204 + causal)
+    for trial in range(300):
+        items = fwd_items(rng, causal)
+        m = FwdModel(rng, items)
+        assert m.run(), f"schedule {trial} (items {items}) hung"
+        assert not m.errors, f"schedule {trial} (items {items}): {m.errors[:3]}"
+
+
+def test_forward_single_block_sparse_items():
+    """A block-sparse CTA runs one item with n0 = n1 key tiles, none at all
+    included (both groups store O = 0 and free their accumulators)."""
+    rng = random.Random(11)
+    for n in [0, 1, 2, 5]:
+        for _ in range(50):
+            m = FwdModel(rng, [(n, n)])
+            assert m.run() and not m.errors, (n, m.errors[:3])
+
+
+def test_forward_model_sees_scores_committed_before_p_is_read():
+    """Sensitivity: a group's next scores issued before its P V (the order
+    the bursts exist to keep) overwrite a P that P V has not read."""
+
+    class EarlyScores(FwdModel):
+        def mma(self):
+            for cond in super().mma():
+                # move every "S" of group 0 ahead of the "PV" queued just before it
+                q = self.queue
+                for i in range(1, len(q)):
+                    if q[i][0] == "S" and q[i][1] == 0 and q[i - 1][0] == "commit" \
+                            and i >= 2 and q[i - 2][0] == "PV" and q[i - 2][1] == 0:
+                        q[i - 2], q[i] = q[i], q[i - 2]
+                yield cond
+
+    rng = random.Random(13)
+    bad = 0
+    for _ in range(100):
+        m = EarlyScores(rng, fwd_items(rng, True))
         bad += (not m.run()) or bool(m.errors)
     assert bad > 0
