@@ -3,10 +3,13 @@
 Names and argument order follow ``include/fa.h``.  Tensors must be CUDA bf16
 (inputs/outputs) or fp32 (lse, D) and contiguous; the functions allocate the
 outputs with PyTorch when they are not given.  Calls are asynchronous on the
-current PyTorch stream unless ``stream`` is given.
+current PyTorch stream of the tensors' device unless ``stream`` is given.  All
+tensors of one call must live on one GPU; that GPU is made current for the
+call (the library launches on the current device).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -120,6 +123,29 @@ def _on_device(t) -> bool:
     return bool(t.is_cuda)
 
 
+def _device_index(t) -> int:
+    return t.get_device()
+
+
+def _one_device(*named):
+    """The device index shared by every (tensor, name) given (None entries
+    skipped): a tensor on another GPU would be read or written through an
+    address the launching GPU may not map."""
+    dev = _device_index(named[0][0])
+    for t, nm in named[1:]:
+        if t is not None and _device_index(t) != dev:
+            raise ValueError(f"{nm} is on device {_device_index(t)}, the call's other tensors "
+                             f"on device {dev}")
+    return dev
+
+
+def _device_guard(dev: int):
+    """Makes device `dev` current for a library call when it is not already."""
+    if dev < 0 or dev == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
+
+
 def _check(t, name, dtype, shape=None):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -160,9 +186,11 @@ def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, o=None
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check(o, "o", torch.bfloat16, (B, H, N, d))
     _check(lse, "lse", torch.float32, (B, H, N))
-    st = library().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                              float(scale), int(bool(causal)),
-                              ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"))
+    with _device_guard(dev):
+        st = library().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                  float(scale), int(bool(causal)),
+                                  ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_forward")
     return o, lse
@@ -192,9 +220,12 @@ def fa_forward_blocksparse(q, k, v, block_mask, causal: bool = False, scale: flo
     _check(o, "o", torch.bfloat16, (B, H, N, d))
     _check(lse, "lse", torch.float32, (B, H, N))
     mp, ms = _mask_args(block_mask, B, H, N)
-    st = library().fa_forward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
-                                          d, float(scale), int(bool(causal)), mp, ms,
-                                          ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"),
+                      (block_mask, "block_mask"))
+    with _device_guard(dev):
+        st = library().fa_forward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                              N, d, float(scale), int(bool(causal)), mp, ms,
+                                              ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_forward_blocksparse")
     return o, lse
@@ -218,11 +249,15 @@ def fa_backward_blocksparse(q, k, v, o, dO, lse, block_mask, causal: bool = Fals
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check_workspace(workspace)
     mp, ms = _mask_args(block_mask, B, H, N)
-    st = library().fa_backward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
-                                           _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
-                                           float(scale), int(bool(causal)), mp, ms,
-                                           _ptr(workspace), workspace.numel(),
-                                           ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse"),
+                      (dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"),
+                      (block_mask, "block_mask"))
+    with _device_guard(dev):
+        st = library().fa_backward_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                               _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N,
+                                               d, float(scale), int(bool(causal)), mp, ms,
+                                               _ptr(workspace), workspace.numel(),
+                                               ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_blocksparse")
     return dq, dk, dv
@@ -244,10 +279,13 @@ def fa_forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0,
     _check(o, "o", torch.bfloat16, (B, H, N, d))
     _check(lse, "lse", torch.float32, (B, H, N))
     mp, ms = (None, 0) if block_mask is None else _mask_args(block_mask, B, H, N)
-    st = library().fa_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                      float(scale), int(bool(causal)), float(p_drop),
-                                      int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp, ms,
-                                      ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"),
+                      (block_mask, "block_mask"))
+    with _device_guard(dev):
+        st = library().fa_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
+                                          d, float(scale), int(bool(causal)), float(p_drop),
+                                          int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp,
+                                          ms, ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_forward_dropout")
     return o, lse
@@ -271,12 +309,16 @@ def fa_backward_dropout(q, k, v, o, dO, lse, p_drop: float, seed: int, offset: i
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check_workspace(workspace)
     mp, ms = (None, 0) if block_mask is None else _mask_args(block_mask, B, H, N)
-    st = library().fa_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
-                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                       int(bool(causal)), float(p_drop),
-                                       int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp, ms,
-                                       _ptr(workspace), workspace.numel(),
-                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse"),
+                      (dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"),
+                      (block_mask, "block_mask"))
+    with _device_guard(dev):
+        st = library().fa_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                           _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                           float(scale), int(bool(causal)), float(p_drop),
+                                           int(seed) & (2**64 - 1), int(offset) & 0xFFFFFFFF, mp,
+                                           ms, _ptr(workspace), workspace.numel(),
+                                           ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_dropout")
     return dq, dk, dv
@@ -294,7 +336,7 @@ def fa_forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: f
     B, H, N, d = q8.shape
     for t, nm, shp in ((q8, "q8", (B, H, N, d)), (k8, "k8", (B, H, N, d)),
                        (vt8, "vt8", (B, H, d, N))):
-        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous():
+        if t.element_size() != 1 or not _on_device(t) or not t.is_contiguous():
             raise TypeError(f"{nm} must be a contiguous one-byte (e4m3) CUDA tensor")
         if tuple(t.shape) != shp:
             raise ValueError(f"{nm} has shape {tuple(t.shape)}, expected {shp}")
@@ -303,10 +345,12 @@ def fa_forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: f
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
     _check(o, "o", torch.bfloat16, (B, H, N, d))
     _check(lse, "lse", torch.float32, (B, H, N))
-    st = library().fa_forward_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), float(q_descale),
-                                  float(k_descale), float(v_descale), _ptr(o), _ptr(lse), B, H,
-                                  N, d, float(scale), int(bool(causal)),
-                                  ctypes.c_void_p(_stream_handle(stream, q8.device)))
+    dev = _one_device((q8, "q8"), (k8, "k8"), (vt8, "vt8"), (o, "o"), (lse, "lse"))
+    with _device_guard(dev):
+        st = library().fa_forward_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), float(q_descale),
+                                      float(k_descale), float(v_descale), _ptr(o), _ptr(lse), B,
+                                      H, N, d, float(scale), int(bool(causal)),
+                                      ctypes.c_void_p(_stream_handle(stream, q8.device)))
     if st != FA_OK:
         raise FaError(st, "fa_forward_fp8")
     return o, lse
@@ -395,9 +439,14 @@ def fa_decode(q, k, v, causal: bool = False, scale: float | None = None, o=None,
     need = fa_decode_workspace_size(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = library().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
-                             float(scale), int(bool(causal)), _ptr(workspace), workspace.numel(),
-                             ctypes.c_void_p(_stream_handle(stream, q.device)))
+    _check_workspace(workspace)
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"),
+                      (workspace, "workspace"))
+    with _device_guard(dev):
+        st = library().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                 float(scale), int(bool(causal)), _ptr(workspace),
+                                 workspace.numel(),
+                                 ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_decode")
     return o, lse
@@ -414,8 +463,10 @@ def fa_backward_preprocess(o, dO, D=None, stream=None):
     if D is None:
         D = torch.empty((B, H, N), dtype=torch.float32, device=o.device)
     _check(D, "D", torch.float32, (B, H, N))
-    st = library().fa_backward_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d,
-                                          ctypes.c_void_p(_stream_handle(stream, o.device)))
+    dev = _one_device((o, "o"), (dO, "dO"), (D, "D"))
+    with _device_guard(dev):
+        st = library().fa_backward_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d,
+                                              ctypes.c_void_p(_stream_handle(stream, o.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_preprocess")
     return D
@@ -438,10 +489,13 @@ def fa_backward(q, k, v, o, dO, lse, causal: bool = False, scale: float | None =
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check_workspace(workspace)
-    st = library().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
-                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                               int(bool(causal)), _ptr(workspace), workspace.numel(),
-                               ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse"),
+                      (dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"))
+    with _device_guard(dev):
+        st = library().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                   int(bool(causal)), _ptr(workspace), workspace.numel(),
+                                   ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward")
     return dq, dk, dv
@@ -460,10 +514,13 @@ def fa_backward_noalloc(q, k, v, o, dO, lse, causal: bool = False, scale: float 
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check_grads(dq, dk, dv, (B, H, N, d))
-    st = library().fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
-                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                       int(bool(causal)),
-                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse"),
+                      (dq, "dq"), (dk, "dk"), (dv, "dv"))
+    with _device_guard(dev):
+        st = library().fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                           _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                           float(scale), int(bool(causal)),
+                                           ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_noalloc")
     return dq, dk, dv
@@ -482,10 +539,13 @@ def fa_backward_dkdv(q, k, v, dO, lse, D, causal: bool = False, scale: float | N
     dv = torch.empty_like(v) if dv is None else dv
     _check(dk, "dk", torch.bfloat16, (B, H, N, d))
     _check(dv, "dv", torch.bfloat16, (B, H, N, d))
-    st = library().fa_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
-                                    _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                    int(bool(causal)),
-                                    ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (dO, "dO"), (lse, "lse"), (D, "D"),
+                      (dk, "dk"), (dv, "dv"))
+    with _device_guard(dev):
+        st = library().fa_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
+                                        _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                        int(bool(causal)),
+                                        ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_dkdv")
     return dk, dv
@@ -502,9 +562,12 @@ def fa_backward_dq(q, k, v, dO, lse, D, causal: bool = False, scale: float | Non
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     _check(dq, "dq", torch.bfloat16, (B, H, N, d))
-    st = library().fa_backward_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
-                                  _ptr(dq), B, H, N, d, float(scale), int(bool(causal)),
-                                  ctypes.c_void_p(_stream_handle(stream, q.device)))
+    dev = _one_device((q, "q"), (k, "k"), (v, "v"), (dO, "dO"), (lse, "lse"), (D, "D"),
+                      (dq, "dq"))
+    with _device_guard(dev):
+        st = library().fa_backward_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
+                                      _ptr(dq), B, H, N, d, float(scale), int(bool(causal)),
+                                      ctypes.c_void_p(_stream_handle(stream, q.device)))
     if st != FA_OK:
         raise FaError(st, "fa_backward_dq")
     return dq

@@ -283,6 +283,8 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
  *    before the next fa_host_wait produce stale outputs, and only that
  *    fa_host_wait's FA_ERR_DEVICE_TIMEOUT reports it.
  *  - fa_host_plan_destroy: waits, then frees the plan (NULL is a no-op).
+ *  - A plan holds unguarded step state (the next slot, the slots' events):
+ *    one thread at a time may call it.  Different plans are independent.
  * Argument errors as for fa_forward; NULL pointers give FA_ERR_NULL.
  */
 typedef struct fa_host_plan fa_host_plan;
