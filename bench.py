@@ -534,13 +534,16 @@ def kernel_table(w, causal, per_kernel_ms, steps, peak, hbm_gbs, mufu_peak):
     return out
 
 
-def secondary_record(fa, name, dev, stream, steps, peaks, mufu_peak):
+def secondary_record(fa, name, dev, stream, steps, peaks, mufu_peak, causal=None, flush=False):
     """Forward and backward TFLOP/s of another workload, timed in this run on
-    resident inputs (its own warm-up; inputs larger than L2)."""
+    resident inputs (its own warm-up).  Inputs larger than L2, or with
+    `flush`, L2 rewritten (256 MB) before every step."""
     w = {**WORKLOADS, **SCALING_WORKLOADS}[name]
-    causal = w.causal[0]
+    causal = w.causal[0] if causal is None else causal
     step, names = make_step(fa, w, causal, dev, stream)
-    per = time_kernels(fa, step, names, steps, 3, dev, stream)
+    fbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+    per = time_kernels(fa, step, names, steps, 3, dev, stream, flush=fbuf)
+    del fbuf
     f_fwd, f_bwd = flops(w, causal)
     fwd_ms = per["fwd"] / steps
     bwd_ms = sum(per[n] for n in names[1:]) / steps
@@ -555,7 +558,8 @@ def secondary_record(fa, name, dev, stream, steps, peaks, mufu_peak):
             "step_tflops": (f_fwd + f_bwd) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
             "ms_per_step": fwd_ms + bwd_ms, "peak_tflops": peak,
             "kernels": kernel_table(w, causal, per, steps, peak, peaks["hbm_gbs"], mufu_peak),
-            "l2": "inputs larger than L2"}
+            "l2": ("flushed before every step (256 MB buffer rewritten)" if flush
+                   else "inputs larger than L2")}
 
 
 def short_record(fa, name, dev, stream, steps, peaks, mufu_peak):
@@ -584,6 +588,107 @@ def short_record(fa, name, dev, stream, steps, peaks, mufu_peak):
             "step_tflops": (f_fwd + (f_bwd if w.backward else 0.0)) / (ms * 1e-3) / 1e12,
             "kernels": kernel_table(w, causal, per, steps, peaks["bf16_tflops"],
                                     peaks["hbm_gbs"], mufu_peak)}
+
+
+def timed_variant(fa, step, steps, warmup, dev, stream):
+    """Mean forward and backward ms of a variant_step over `steps` steps after
+    `warmup` untimed ones, a new Philox offset every step."""
+    for i in range(warmup):
+        step(offset=i)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for s_ in range(steps):
+        evs[s_][0].record(stream)
+        step(evs[s_], offset=warmup + s_)
+    torch.cuda.synchronize(dev)
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    return (sum(e[0].elapsed_time(e[1]) for e in evs) / steps,
+            sum(e[1].elapsed_time(e[2]) for e in evs) / steps)
+
+
+def timed_launches(fa, step, steps, warmup, dev, stream):
+    """Mean ms per step(i) over `steps` steps after `warmup` untimed ones."""
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st, detail = fa.fa_get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {st} {detail:#x}")
+    return e0.elapsed_time(e1) / steps
+
+
+NEXT_ROW_STEPS = 10
+NEXT_ROW_BAND = "band:8:1"
+NEXT_ROW_DECODE = ("causal_b1h32n32768d128_qk2", 16)
+
+
+def next_rows_record(fa, inputs, dev, stream, peaks, steps=NEXT_ROW_STEPS):
+    """The widened rows, timed in this run on resident inputs larger than L2
+    (3 warm-up steps each): dropout (p = 0.1, a new Philox offset per step,
+    causal) and block-sparse (NEXT_ROW_BAND, non-causal) forward + backward
+    and the e4m3 forward (causal) on the 8K workload; decode with 16 query
+    rows against the 32-head 32K-token cache.  TFLOP/s count the method's
+    work on the elements kept (block-sparse: kept tiles); `inputs` are the 8K
+    workload's host tensors (None: drawn here)."""
+    w = WORKLOADS[DEFAULT_WORKLOAD]
+    peak = peaks["bf16_tflops"]
+    if inputs is None:
+        inputs = make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+    tensors = tuple(t.to(dev) for t in inputs)
+    dense = float(w.B * w.H * w.N * w.N)
+
+    def rates(E, fwd_ms, bwd_ms):
+        f_fwd, f_bwd = 4.0 * w.d * E, 10.0 * w.d * E
+        return {"fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                "step_tflops": (f_fwd + f_bwd) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                "fwd_frac_of_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
+                "ms_per_step": fwd_ms + bwd_ms}
+
+    out = {"steps": steps, "peak_tflops": peak}
+    step = variant_step(fa, w, True, tensors, None, 0.1, dev, stream)
+    out["dropout"] = {"workload": w.name, "causal": True, "p": 0.1,
+                      "rng": "Philox4x32-10, new offset per step",
+                      **rates(0.5 * dense, *timed_variant(fa, step, steps, 3, dev, stream))}
+    mask_cpu = band_mask(NEXT_ROW_BAND, w.N)
+    E = kept_elements(mask_cpu, w.N, False) * w.B * w.H
+    step = variant_step(fa, w, False, tensors, mask_cpu.to(dev), 0.0, dev, stream)
+    out["blocksparse"] = {"workload": w.name, "causal": False, "block_mask": NEXT_ROW_BAND,
+                          "kept_fraction": E / dense,
+                          **rates(E, *timed_variant(fa, step, steps, 3, dev, stream))}
+    del step, tensors
+    torch.cuda.empty_cache()
+
+    step = fp8_step(fa, w, True, dev, stream)
+    ms = timed_launches(fa, lambda i: step(), steps, 3, dev, stream)
+    tf = flops(w, True)[0] / (ms * 1e-3) / 1e12
+    out["fp8_forward"] = {"workload": w.name, "causal": True, "tflops": tf,
+                          "frac_of_fp8_peak": tf / (2.0 * peak), "ms_per_launch": ms,
+                          "peak": "fp8 = 2 x burst bf16 (the nominal fp8 : bf16 ratio)"}
+    del step
+    torch.cuda.empty_cache()
+
+    name, Nq = NEXT_ROW_DECODE
+    wd = WORKLOADS[name]
+    qkv = tuple(t.to(dev) for t in make_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, wd.qk_mult,
+                                               with_dO=False)[:3])
+    step, nbytes, n_caches, _ = decode_step(fa, wd, qkv, Nq, dev, stream)
+    ms = timed_launches(fa, step, steps, 3, dev, stream)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["decode"] = {"workload": f"decode_q{Nq}_{name}", "Nq": Nq, "Nk": wd.N, "hbm_gbs": gbs,
+                     "hbm_frac": gbs / peaks["hbm_gbs"], "us_per_step": ms * 1e3,
+                     "cache_copies": n_caches}
+    del step, qkv
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -698,15 +803,19 @@ def run_ours(args, world, rank, local):
     roof["ms_per_launch"] = dom_ms
 
     # headline-adjacent workloads, timed in this run (rank 0, one GPU)
-    secondary = short = None
+    secondary = short = config2 = next_rows = None
     if rank == 0 and world == 1 and not args.no_secondary:
         del step
         torch.cuda.empty_cache()
         sec_steps = max(3, min(args.steps, 20))
         secondary = secondary_record(fa, "causal_b1h32n32768d128_qk2", dev, stream, sec_steps,
                                      peaks, mufu_peak)
+        config2 = [secondary_record(fa, "b4h16n2048d64", dev, stream, sec_steps, peaks,
+                                    mufu_peak, causal=c, flush=True) for c in (True, False)]
         short = [short_record(fa, n, dev, stream, 50, peaks, mufu_peak)
                  for n in ("fwd_b1h2n256d64", "short_b64h12n512d64")]
+        next_rows = next_rows_record(fa, inputs if w.name == DEFAULT_WORKLOAD else None, dev,
+                                     stream, peaks)
 
     # end to end through the C ABI's host-buffer runtime (fa_host_step): every
     # step copies its inputs in from pinned host memory and its outputs
@@ -786,7 +895,8 @@ def run_ours(args, world, rank, local):
             "peak_tflops": peak, "peak_source": f"{peak_kind} bf16, {peak_src}",
             "kernels": kernels, "roofline": roof, "diagnostics": diag, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk,
-            "secondary": secondary, "short_sequence": short,
+            "secondary": secondary, "config2": config2, "short_sequence": short,
+            "next_rows": next_rows,
         }
         print(json.dumps(line), flush=True)
     return 0
@@ -797,18 +907,13 @@ E2E_MIN_SECONDS = 1.0
 E2E_MAX_STEPS = 4000
 
 
-def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
-    """Block-sparse and / or dropout step: fa_forward_blocksparse +
-    fa_backward_blocksparse (--block-mask), fa_forward_dropout +
-    fa_backward_dropout (--dropout, with the block mask if one is given)."""
+def variant_step(fa, w, causal, tensors, mask, p_drop, dev, stream, seed=0x5EED):
+    """step(ev=None, offset=0) of the block-sparse and / or dropout path:
+    fa_forward_blocksparse + fa_backward_blocksparse (mask given, p_drop 0),
+    fa_forward_dropout + fa_backward_dropout (p_drop > 0, with the mask if
+    given) at Philox offset `offset`; ev[1] is recorded after the forward and
+    ev[2] after the backward."""
     q, k, v, dO = tensors
-    if args.block_mask:
-        mask_cpu = band_mask(args.block_mask, w.N)
-        mask = mask_cpu.to(dev)
-    else:
-        mask_cpu = mask = None
-    p_drop = args.dropout or 0.0
-    seed = 0x5EED
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -833,6 +938,22 @@ def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
                                        dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
+
+    return step
+
+
+def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
+    """Block-sparse and / or dropout step: fa_forward_blocksparse +
+    fa_backward_blocksparse (--block-mask), fa_forward_dropout +
+    fa_backward_dropout (--dropout, with the block mask if one is given)."""
+    q, k, v, dO = tensors
+    if args.block_mask:
+        mask_cpu = band_mask(args.block_mask, w.N)
+        mask = mask_cpu.to(dev)
+    else:
+        mask_cpu = mask = None
+    p_drop = args.dropout or 0.0
+    step = variant_step(fa, w, causal, (q, k, v, dO), mask, p_drop, dev, stream)
 
     for i in range(args.warmup):
         step(offset=i)
@@ -889,15 +1010,11 @@ def run_variant(args, world, rank, local, fa, w, causal, tensors, stream, dev):
     return 0
 
 
-def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
-    """e4m3 forward step: fa_forward_fp8 on the workload's q, k, v quantised
-    per tensor (fa_inputs.make_fp8_inputs).  Tensor-bound: FLOPs of the two
-    products (4 N^2 d per head, halved when causal) against the fp8 peak =
-    measured bf16 peak x 2 (the nominal fp8 : bf16 ratio)."""
+def fp8_step(fa, w, causal, dev, stream):
+    """step() of the e4m3 forward on the workload's q, k, v quantised per
+    tensor (fa_inputs.make_fp8_inputs; V transposed per head); d = 128."""
     from fa_inputs import make_fp8_inputs
 
-    if w.d != 128:
-        raise SystemExit("--fp8 needs a d = 128 workload")
     q8, k8, _, vt8, ds = make_fp8_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
     q, k, vt = (t.view(torch.uint8).to(dev) for t in (q8, k8, vt8))
     del q8, k8, vt8
@@ -908,6 +1025,17 @@ def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
         fa.fa_forward_fp8(q, k, vt, *ds, causal=causal, scale=w.scale, o=o, lse=lse,
                           stream=stream)
 
+    return step
+
+
+def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
+    """e4m3 forward step: fa_forward_fp8 on the workload's q, k, v quantised
+    per tensor (fa_inputs.make_fp8_inputs).  Tensor-bound: FLOPs of the two
+    products (4 N^2 d per head, halved when causal) against the fp8 peak =
+    measured bf16 peak x 2 (the nominal fp8 : bf16 ratio)."""
+    if w.d != 128:
+        raise SystemExit("--fp8 needs a d = 128 workload")
+    step = fp8_step(fa, w, causal, dev, stream)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -951,18 +1079,18 @@ def run_fp8(args, world, rank, local, fa, w, causal, stream, dev):
     return 0
 
 
-def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
-    """Decode step: the last --decode query rows against the whole key/value
-    cache of the workload (causal: query i at position N - Nq + i).  HBM-bound:
-    reported as GB/s of algorithmic bytes (K, V, q read once; o, lse written)."""
+def decode_step(fa, w, tensors, Nq, dev, stream):
+    """step(i) of the decode path: the last Nq query rows of the workload
+    against its whole key/value cache (causal: query i at position N - Nq + i),
+    rotating over enough copies of the cache that the inputs of consecutive
+    steps exceed L2.  Returns (step, algorithmic bytes per step (K, V, q read
+    once; o, lse written), copies, MB per cache)."""
     q_full, k, v = tensors
-    Nq = int(args.decode)
     q = q_full[:, :, w.N - Nq:].contiguous()
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
     ws = torch.empty(fa.fa_decode_workspace_size(w.B, w.H, Nq, w.N, w.d), dtype=torch.uint8,
                      device=dev)
-    # inputs larger than L2 between steps: rotate over copies of the cache
     copies = max(1, int((300e6 // (2 * k.numel() * 2)) + 1))
     caches = [(k, v)] + [(k.clone(), v.clone()) for _ in range(copies - 1)]
 
@@ -971,6 +1099,16 @@ def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
         fa.fa_decode(q, kk, vv, causal=True, scale=w.scale, o=o, lse=lse, workspace=ws,
                      stream=stream)
 
+    nbytes = (2 * k.numel() + 2 * q.numel()) * 2 + lse.numel() * 4
+    return step, nbytes, len(caches), 2 * k.numel() * 2 / 1e6
+
+
+def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
+    """Decode step: the last --decode query rows against the whole key/value
+    cache of the workload (causal: query i at position N - Nq + i).  HBM-bound:
+    reported as GB/s of algorithmic bytes (K, V, q read once; o, lse written)."""
+    Nq = int(args.decode)
+    step, nbytes, n_caches, cache_mb = decode_step(fa, w, tensors, Nq, dev, stream)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
@@ -989,13 +1127,12 @@ def run_decode(args, world, rank, local, fa, w, tensors, stream, dev):
     if st != 0:
         raise RuntimeError(f"device error: {st} {detail:#x}")
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    nbytes = (2 * k.numel() + 2 * q.numel()) * 2 + lse.numel() * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
     peaks, peak_src = read_peaks()
     if rank == 0:
         cfg = {"workload": f"decode_q{Nq}_{w.name}", "B": w.B, "H": w.H, "Nq": Nq, "Nk": w.N,
                "d": w.d, "causal": True,
-               "l2": f"{len(caches)} rotating copies of the K/V cache ({2 * k.numel() * 2 / 1e6:.0f} MB each)"}
+               "l2": f"{n_caches} rotating copies of the K/V cache ({cache_mb:.0f} MB each)"}
         line = {
             "metric": "attention decode step HBM GB/s (K/V cache read once)", "value": world * gbs,
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -141,3 +141,135 @@ def test_clock_summary_counts_samples_in_the_timed_region():
     assert s["sm_mhz"] == 2070.0 and s["sm_mhz_min"] == 2040.0
     assert s["reasons"] == ["sw_power_cap"]
     assert s["power_w_max"] == 1000.0
+
+
+class StubRun:
+    """The real binding over a stub library that records its calls, CPU
+    tensors accepted as device tensors, CUDA events that report 0.5 ms per
+    interval, and small stand-ins for the 8K and 32K workloads."""
+
+    def __init__(self, monkeypatch):
+        import types
+
+        import torch
+        from exact_io_aware_16_gb300 import _binding as bd
+        from fa_inputs import Workload
+
+        calls = self.calls = []
+
+        class Stub:
+            def __getattr__(self, name):
+                def fn(*a):
+                    calls.append(name)
+                    if name == "fa_backward_workspace_size":
+                        return 4 * a[0] * a[1] * a[2]
+                    if name == "fa_decode_workspace_size":
+                        return 4096
+                    return 0
+                return fn
+
+        class Event:
+            def __init__(self, enable_timing=False):
+                pass
+
+            def record(self, stream=None):
+                pass
+
+            def elapsed_time(self, other):
+                return 0.5
+
+        monkeypatch.setattr(bd, "library", lambda: Stub())
+        monkeypatch.setattr(bd, "_on_device", lambda t: True)
+        dec_name = bench.NEXT_ROW_DECODE[0]
+        self.small = {
+            bench.DEFAULT_WORKLOAD: Workload(bench.DEFAULT_WORKLOAD, 1, 2, 1024, 128, (True,)),
+            dec_name: Workload(dec_name, 1, 2, 2048, 128, (True,), qk_mult=2.0)}
+        monkeypatch.setattr(bench, "WORKLOADS", self.small)
+        monkeypatch.setattr(bench.torch.cuda, "Event", Event)
+        monkeypatch.setattr(bench.torch.cuda, "synchronize", lambda *a: None)
+        monkeypatch.setattr(bench, "ClockSampler", lambda dev: types.SimpleNamespace(
+            start=lambda: None, stop=lambda: None, mark_load=lambda: None,
+            mark_done=lambda: None))
+        fa = types.SimpleNamespace(**{n: getattr(bd, n) for n in dir(bd) if n.startswith("fa_")})
+        fa.fa_get_device_error = lambda stream=None: (0, 0)
+        self.fa = fa
+        self.dev = torch.device("cpu")
+
+
+def test_next_rows_record_drives_every_widened_row(monkeypatch):
+    """The default line's record of the widened rows: every row's entry
+    point is launched for its warm-up and timed steps, and the rates follow
+    from the FLOP and byte counts."""
+    run = StubRun(monkeypatch)
+    calls, small, fa = run.calls, run.small, run.fa
+    dec_name = bench.NEXT_ROW_DECODE[0]
+
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0}
+    steps = 2
+    rec = bench.next_rows_record(fa, None, run.dev, 0, peaks, steps=steps)
+
+    n = 3 + steps
+    for name in ("fa_forward_dropout", "fa_backward_dropout", "fa_forward_blocksparse",
+                 "fa_backward_blocksparse", "fa_forward_fp8", "fa_decode"):
+        assert calls.count(name) == n, (name, calls.count(name))
+    w, wd = small[bench.DEFAULT_WORKLOAD], small[dec_name]
+    E = 0.5 * w.B * w.H * w.N * w.N
+    drop = rec["dropout"]
+    assert drop["ms_per_step"] == pytest.approx(1.0)
+    assert drop["fwd_tflops"] == pytest.approx(4 * w.d * E / 0.5e-3 / 1e12)
+    assert drop["bwd_tflops"] == pytest.approx(10 * w.d * E / 0.5e-3 / 1e12)
+    bs = rec["blocksparse"]
+    kept = bench.kept_elements(bench.band_mask(bench.NEXT_ROW_BAND, w.N), w.N, False)
+    assert bs["kept_fraction"] == pytest.approx(kept / (w.N * w.N))
+    assert bs["step_tflops"] == pytest.approx(14 * w.d * kept * w.B * w.H / 1e-3 / 1e12)
+    assert rec["fp8_forward"]["ms_per_launch"] == pytest.approx(0.5 / steps)
+    assert rec["fp8_forward"]["frac_of_fp8_peak"] == pytest.approx(
+        rec["fp8_forward"]["tflops"] / 4000.0)
+    dec = rec["decode"]
+    # K and V read once, q read and o written (bf16), lse written (fp32)
+    nbytes = 2 * (2 * wd.B * wd.H * wd.N * wd.d) + 2 * (2 * wd.B * wd.H * 16 * wd.d) + \
+        4 * wd.B * wd.H * 16
+    assert dec["us_per_step"] == pytest.approx(1e3 * 0.5 / steps)
+    assert dec["hbm_gbs"] == pytest.approx(nbytes / (0.5 / steps * 1e-3) / 1e9)
+
+
+@pytest.mark.parametrize("flag", ["dropout", "block_mask", "both", "fp8", "decode"])
+def test_flag_runners_print_one_line(monkeypatch, capsys, flag):
+    """bench.py --dropout / --block-mask / --fp8 / --decode on the stub run:
+    each launches its entry points for every warm-up and timed step and
+    prints one JSON line whose rate follows from the 0.5 ms intervals."""
+    run = StubRun(monkeypatch)
+    w = run.small[bench.DEFAULT_WORKLOAD]
+    args = argparse.Namespace(steps=3, warmup=2, dropout=None, block_mask=None, decode=None)
+    tensors = make_small_inputs(w)
+    if flag in ("dropout", "both"):
+        args.dropout = 0.1
+    if flag in ("block_mask", "both"):
+        args.block_mask = "band:2:1"
+    if flag == "fp8":
+        assert bench.run_fp8(args, 1, 0, 0, run.fa, w, True, 0, run.dev) == 0
+        want = {"fa_forward_fp8": 5}
+    elif flag == "decode":
+        args.decode = 4
+        assert bench.run_decode(args, 1, 0, 0, run.fa, w, tensors[:3], 0, run.dev) == 0
+        want = {"fa_decode": 5}
+    else:
+        assert bench.run_variant(args, 1, 0, 0, run.fa, w, True, tensors, 0, run.dev) == 0
+        kind = "dropout" if args.dropout else "blocksparse"
+        want = {f"fa_forward_{kind}": 5, f"fa_backward_{kind}": 5}
+    for name, count in want.items():
+        assert run.calls.count(name) == count, (name, run.calls)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["value"] > 0 and line["n_gpus"] == 1 and line["steps"] == 3
+    if flag == "decode":
+        assert line["ms_per_step"] == pytest.approx(0.5 / 3)
+    elif flag == "fp8":
+        assert line["ms_per_step"] == pytest.approx(0.5)
+    else:
+        assert line["ms_per_step"] == pytest.approx(1.0)
+
+
+def make_small_inputs(w):
+    from fa_inputs import make_inputs
+
+    return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)

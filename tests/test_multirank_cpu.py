@@ -42,7 +42,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a threaded process
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
