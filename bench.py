@@ -1168,7 +1168,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the 32K and short-sequence records timed after the main one")
+                    help="skip the records timed after the main one (32K, B4 H16 N2048 d64, "
+                         "short sequences, the widened rows)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
