@@ -12,7 +12,8 @@ its own "scores ready" and "P ready" barrier for that reason.
 
 `Model` replays the protocol of csrc/fa_bwd.cu (the dK/dV kernel; the dQ
 kernel's is the same with B = P K in place of dV and dQ~ in place of dK) and
-`FwdModel` that of csrc/fa_fwd.cu, both with true parity semantics: the
+`FwdModel` that of csrc/fa_fwd.cu and `DecodeModel` that of the decode kernel
+(csrc/fa_decode.cu), all with true parity semantics: the
 tensor core completes products in issue order, a commit's arrival fires when
 the products issued before it have completed, tile loads land in any order,
 and every role advances at random.  The compute side is two warps that each
@@ -586,5 +587,177 @@ def test_forward_model_sees_scores_committed_before_p_is_read():
     bad = 0
     for _ in range(100):
         m = EarlyScores(rng, fwd_items(rng, True))
+        bad += (not m.run()) or bool(m.errors)
+    assert bad > 0
+
+
+class DecodeModel:
+    """The decode kernel's split: one item (n key tiles of one head and key
+    range), one softmax warp, Q resident, K and V streamed through a ring of
+    `stages`, two score buffers (tile t in buffer t & 1, each with its own
+    scores-ready barrier) and the next-but-one tile's scores issued after the
+    P V that frees their buffer."""
+
+    def __init__(self, rng, n, stages):
+        self.rng, self.n, self.R = rng, n, stages
+        B = Barrier
+        self.q_full = B(1)
+        self.k_full, self.k_empty = [B(1) for _ in range(stages)], [B(1) for _ in range(stages)]
+        self.v_full, self.v_empty = [B(1) for _ in range(stages)], [B(1) for _ in range(stages)]
+        self.s_full = [B(1), B(1)]
+        self.p_ready, self.pv_done = B(1), B(1)
+        self.queue, self.loads = [], []
+        self.q_in = False
+        self.k_tile, self.v_tile = [None] * stages, [None] * stages
+        self.sbuf = [None, None]  # ("S" | "P", tile)
+        self.p_read = [True, True]
+        self.o = 0  # P V products accumulated
+        self.errors = []
+
+    def tensor_step(self):
+        kind, *arg = self.queue.pop(0)
+        if kind == "commit":
+            arg[0].arrive()
+            return
+        t = arg[0]
+        b, st = t & 1, t % self.R
+        if kind == "S":
+            if not self.q_in or self.k_tile[st] != t:
+                self.errors.append(f"S({t}) read K tile {self.k_tile[st]}")
+            if not self.p_read[b]:
+                self.errors.append(f"S({t}) overwrote P{self.sbuf[b]} before P V read it")
+            self.sbuf[b] = ("S", t)
+        else:  # PV
+            if self.sbuf[b] != ("P", t) or self.v_tile[st] != t:
+                self.errors.append(f"PV({t}) read {self.sbuf[b]}, V tile {self.v_tile[st]}")
+            if self.o != t:
+                self.errors.append(f"PV({t}) accumulated onto {self.o} products")
+            self.p_read[b] = True
+            self.o = t + 1
+
+    def producer(self):
+        self.loads.append(("Q", 0))
+        for t in range(self.n):
+            st, ph = t % self.R, (t // self.R) & 1
+            yield lambda st=st, ph=ph: self.k_empty[st].done(ph ^ 1)
+            self.loads.append(("K", t))
+            yield lambda st=st, ph=ph: self.v_empty[st].done(ph ^ 1)
+            self.loads.append(("V", t))
+
+    def land(self, load):
+        kind, t = load
+        if kind == "Q":
+            self.q_in = True
+            self.q_full.arrive()
+        elif kind == "K":
+            self.k_tile[t % self.R] = t
+            self.k_full[t % self.R].arrive()
+        else:
+            self.v_tile[t % self.R] = t
+            self.v_full[t % self.R].arrive()
+
+    def issue_s(self, t):
+        self.queue += [("S", t), ("commit", self.s_full[t & 1]),
+                       ("commit", self.k_empty[t % self.R])]
+
+    def mma(self):
+        yield lambda: self.q_full.done(0)
+        yield lambda: self.k_full[0].done(0)
+        self.issue_s(0)
+        if self.n > 1:
+            yield lambda: self.k_full[1 % self.R].done((1 // self.R) & 1)
+            self.issue_s(1)
+        for t in range(self.n):
+            yield lambda t=t: self.p_ready.done(t & 1)
+            yield lambda t=t: self.v_full[t % self.R].done((t // self.R) & 1)
+            self.queue += [("PV", t), ("commit", self.pv_done),
+                           ("commit", self.v_empty[t % self.R])]
+            if t + 2 < self.n:
+                u = t + 2
+                yield lambda u=u: self.k_full[u % self.R].done((u // self.R) & 1)
+                self.issue_s(u)
+
+    def softmax(self):
+        for t in range(self.n):
+            yield lambda t=t: self.s_full[t & 1].done((t >> 1) & 1)
+            if self.sbuf[t & 1] != ("S", t):
+                self.errors.append(f"softmax {t} read {self.sbuf[t & 1]}")
+            yield None
+            self.sbuf[t & 1] = ("P", t)
+            self.p_read[t & 1] = False
+            if t > 0:  # P V of the previous tile done before O is rescaled
+                yield lambda t=t: self.pv_done.done((t - 1) & 1)
+                if self.o != t:
+                    self.errors.append(f"softmax {t} rescaled O with {self.o} products")
+                yield None
+                if self.o != t:
+                    self.errors.append(f"O changed under the rescale at {t}")
+            self.p_ready.arrive()
+        yield lambda: self.pv_done.done((self.n - 1) & 1)
+        if self.o != self.n:
+            self.errors.append(f"epilogue read O with {self.o} of {self.n} products")
+
+    def run(self):
+        roles = {"producer": self.producer(), "mma": self.mma(), "softmax": self.softmax()}
+        waiting = {name: None for name in roles}
+        finished = set()
+        for _ in range(100000):
+            enabled = [r for r in roles if r not in finished
+                       and (waiting[r] is None or waiting[r]())]
+            if self.queue:
+                enabled.append("tensor")
+            if self.loads:
+                enabled.append("tma")
+            if not enabled:
+                break
+            pick = self.rng.choice(enabled)
+            if pick == "tensor":
+                self.tensor_step()
+            elif pick == "tma":
+                self.land(self.loads.pop(self.rng.randrange(len(self.loads))))
+            else:
+                try:
+                    waiting[pick] = next(roles[pick])
+                except StopIteration:
+                    finished.add(pick)
+                    waiting[pick] = None
+        return finished == set(roles) and not self.queue and not self.loads
+
+
+@pytest.mark.parametrize("stages", [2, 4], ids=["d128", "d64"])
+def test_decode_protocol_never_hangs_and_reads_its_own_tile(stages):
+    rng = random.Random(20261205 + stages)
+    for trial in range(300):
+        n = rng.randint(1, 9)
+        m = DecodeModel(rng, n, stages)
+        assert m.run(), f"schedule {trial} (n = {n}) hung"
+        assert not m.errors, f"schedule {trial} (n = {n}): {m.errors[:3]}"
+
+
+def test_decode_model_sees_scores_issued_into_a_busy_buffer():
+    """Sensitivity: issuing tile t + 2's scores before P V(t) overwrites P(t)."""
+
+    class Early(DecodeModel):
+        def mma(self):
+            yield lambda: self.q_full.done(0)
+            yield lambda: self.k_full[0].done(0)
+            self.issue_s(0)
+            if self.n > 1:
+                yield lambda: self.k_full[1 % self.R].done((1 // self.R) & 1)
+                self.issue_s(1)
+            for t in range(self.n):
+                if t + 2 < self.n:
+                    u = t + 2
+                    yield lambda u=u: self.k_full[u % self.R].done((u // self.R) & 1)
+                    self.issue_s(u)
+                yield lambda t=t: self.p_ready.done(t & 1)
+                yield lambda t=t: self.v_full[t % self.R].done((t // self.R) & 1)
+                self.queue += [("PV", t), ("commit", self.pv_done),
+                               ("commit", self.v_empty[t % self.R])]
+
+    rng = random.Random(17)
+    bad = 0
+    for _ in range(100):
+        m = Early(rng, rng.randint(3, 9), 4)
         bad += (not m.run()) or bool(m.errors)
     assert bad > 0
