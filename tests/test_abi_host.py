@@ -189,6 +189,59 @@ def test_decode_validation(lib):
     assert dec(wb=16) == -6
 
 
+def test_split_backward_validation(lib):
+    """The backward's three kernels called one at a time reject bad arguments
+    with the documented codes before anything is launched."""
+    pre = lib.fa_backward_preprocess
+    assert pre(None, FAKE, FAKE, 1, 1, 128, 64, None) == -1
+    assert pre(FAKE, FAKE, None, 1, 1, 128, 64, None) == -1
+    assert pre(FAKE, FAKE, FAKE, 1, 1, 0, 64, None) == -2
+    assert pre(FAKE, FAKE, FAKE, 1, 1, 128, 96, None) == -3
+    assert pre(FAKE, FAKE, FAKE + 4, 1, 1, 128, 64, None) == -4
+
+    def dq(D=FAKE, out=FAKE, d=64, scale=0.125, N=128):
+        return lib.fa_backward_dq(FAKE, FAKE, FAKE, FAKE, FAKE, D, out, 1, 2, N, d, scale, 1,
+                                  None)
+
+    assert dq(D=None) == -1
+    assert dq(out=None) == -1
+    assert dq(N=-3) == -2
+    assert dq(d=80) == -3
+    assert dq(scale=float("nan")) == -2
+    assert dq(out=FAKE + 2) == -4
+
+    def dkdv(dk=FAKE, dv=FAKE, D=FAKE, d=128, scale=0.125):
+        return lib.fa_backward_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, D, dk, dv, 1, 2, 256, d, scale,
+                                    0, None)
+
+    assert dkdv(dk=None) == -1
+    assert dkdv(dv=None) == -1
+    assert dkdv(D=None) == -1
+    assert dkdv(d=256) == -3
+    assert dkdv(scale=0.0) == -2
+    assert dkdv(dv=FAKE + 8) == -4
+
+
+def test_noalloc_validation(lib):
+    """fa_backward_noalloc refuses problems its built-in workspace cannot
+    hold (more than FA_NOALLOC_MAX_ROWS rows) and bad shapes before it does
+    anything else; its remaining checks are fa_backward's."""
+    max_rows = 2097152  # FA_NOALLOC_MAX_ROWS in include/fa.h
+    hdr = open(os.path.join(ROOT, "include", "fa.h")).read()
+    assert f"#define FA_NOALLOC_MAX_ROWS {max_rows}" in hdr
+
+    def na(q=FAKE, B=1, H=2, N=128, d=64):
+        return lib.fa_backward_noalloc(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H,
+                                       N, d, 0.125, 0, None)
+
+    assert na(q=None) == -1
+    assert na(B=0) == -2
+    assert na(N=-1) == -2
+    assert na(d=96) == -3
+    assert na(B=1, H=16, N=max_rows // 16 + 1) == -6  # one row too many
+    assert na(B=2, H=1 << 10, N=1 << 20) == -6  # rows beyond 2^31
+
+
 def test_workspace_size_is_linear_in_n(lib):
     f = lib.fa_backward_workspace_size
     assert f(1, 1, 0, 64) == 0
