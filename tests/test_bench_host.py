@@ -261,6 +261,8 @@ def test_flag_runners_print_one_line(monkeypatch, capsys, flag):
         assert run.calls.count(name) == count, (name, run.calls)
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["value"] > 0 and line["n_gpus"] == 1 and line["steps"] == 3
+    if flag != "decode":  # a few MB of inputs: L2 is flushed, and the line says so
+        assert line["config"]["l2"].startswith("L2 flushed before every step")
     if flag == "decode":
         assert line["ms_per_step"] == pytest.approx(0.5 / 3)
     elif flag == "fp8":
@@ -273,3 +275,16 @@ def make_small_inputs(w):
     from fa_inputs import make_inputs
 
     return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult)
+
+
+def test_l2_label_follows_the_step_size():
+    """The default workload's tensors exceed L2; a workload that fits in L2 is
+    timed with a flush and labelled so (the bench flushes exactly when the
+    label says it does)."""
+    big, small = WORKLOADS["causal_b2h16n8192d128"], WORKLOADS["b4h16n2048d64"]
+    assert bench.step_bytes(big) > bench.L2_BYTES
+    assert bench.workload_config(big, True)["l2"].startswith("inputs larger than L2")
+    assert bench.step_bytes(small) <= bench.L2_BYTES
+    assert bench.workload_config(small, True)["l2"].startswith("L2 flushed")
+    assert bench.l2_flush_buffer(bench.step_bytes(big), "cpu") is None
+    assert bench.l2_flush_buffer(1000, "cpu").numel() == bench.FLUSH_BYTES > bench.L2_BYTES
