@@ -160,3 +160,45 @@ def rounding_bounds(q, k, v, dO, o_ref, scale, causal):
                                              + np.abs(D - Dt)[:, None] * (P @ absK))
             out_v[b, h] = 2.0 ** -8 * (P.T @ np.abs(DO[b, h]))
     return out, out_v
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("delta,N", CASES, ids=[f"delta{int(c[0])}" for c in CASES])
+def test_bounds_cover_the_bf16_replay(delta, N, causal, d):
+    """The dQ and dV bounds hold, with room, for a CPU replay of the kernels'
+    arithmetic at its bf16 rounding points: dS~ = P (dP - D~) and P rounded
+    to bf16 as MMA operands, dQ = scale (dS~ K - (D - D~) B) with B = P K,
+    dV = P^T dO; everything else in fp64."""
+    q, k, v, dO, scale = ramp_inputs(delta, N, d)
+    shape = tuple(q.shape)
+    o_ref, _ = oracle.forward(q, k, v, scale, causal)
+    o_ref = np.asarray(o_ref).reshape(shape)
+    dq_ref, _, dv_ref, _ = oracle.backward(q, k, v, dO, scale, causal)
+    dq_ref, dv_ref = (np.asarray(x, dtype=np.float64).reshape(shape) for x in (dq_ref, dv_ref))
+    dq_b, dv_b = rounding_bounds(q, k, v, dO, o_ref, scale, causal)
+    Q, K, V, DO = (x.double().numpy() for x in (q, k, v, dO))
+    Ob = _bf16(o_ref)
+    worst = {"dQ": 0.0, "dV": 0.0}
+    for b in range(shape[0]):
+        for h in range(shape[1]):
+            S = Q[b, h] @ K[b, h].T * scale
+            if causal:
+                S = np.where(np.tril(np.ones_like(S)) > 0, S, -np.inf)
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            dP = DO[b, h] @ V[b, h].T
+            Dt, D = (DO[b, h] * Ob[b, h]).sum(axis=1), (P * dP).sum(axis=1)
+            dq = scale * (_bf16(P * (dP - Dt[:, None])) @ K[b, h]
+                          - (D - Dt)[:, None] * (_bf16(P) @ K[b, h]))
+            dv = _bf16(P).T @ DO[b, h]
+            for name, got, ref, extra in (("dQ", dq, dq_ref[b, h], dq_b[b, h]),
+                                          ("dV", dv, dv_ref[b, h], dv_b[b, h])):
+                half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 8)
+                r = (np.abs(got - ref) / (2e-2 + extra + half_ulp)).max()
+                worst[name] = max(worst[name], float(r))
+    assert worst["dQ"] <= 0.75 and worst["dV"] <= 0.5, worst
