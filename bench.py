@@ -244,7 +244,13 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        if args.impl == "ours":
+            # each rank on its own GPU before the first collective (a barrier
+            # issued earlier would have to guess the rank's device)
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -716,7 +722,7 @@ def run_ours(args, world, rank, local):
     import exact_io_aware_16_gb300 as fa
     from exact_io_aware_16_gb300 import build as fabuild
 
-    if rank == 0 or not os.path.exists(fabuild.LIB):
+    if rank == 0:  # one build; the other ranks load it after the barrier
         fabuild.build()
     barrier(world)
     torch.cuda.set_device(local)
