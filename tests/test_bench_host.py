@@ -288,3 +288,23 @@ def test_l2_label_follows_the_step_size():
     assert bench.workload_config(small, True)["l2"].startswith("L2 flushed")
     assert bench.l2_flush_buffer(bench.step_bytes(big), "cpu") is None
     assert bench.l2_flush_buffer(1000, "cpu").numel() == bench.FLUSH_BYTES > bench.L2_BYTES
+
+
+def test_nccl_ranks_bind_their_gpu_before_the_group_forms(monkeypatch):
+    """Under torchrun each rank of the CUDA arm takes its own GPU before the
+    NCCL process group forms (no collective has to guess the device); the
+    reference arm joins a gloo group and binds no GPU."""
+    import torch.distributed as dist
+
+    calls = []
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    monkeypatch.setattr(bench.torch.cuda, "set_device", lambda d: calls.append(("set_device", d)))
+    monkeypatch.setattr(dist, "init_process_group",
+                        lambda backend, **kw: calls.append(("init", backend)))
+    assert bench.dist_setup(argparse.Namespace(impl="ours")) == (2, 1, 1)
+    assert calls == [("set_device", 1), ("init", "nccl")]
+    calls.clear()
+    assert bench.dist_setup(argparse.Namespace(impl="reference")) == (2, 1, 1)
+    assert calls == [("init", "gloo")]
