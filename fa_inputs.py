@@ -119,10 +119,6 @@ def dequantize(x8, descale: float):
     return x8.to(torch.float64) * float(descale)
 
 
-def workload_inputs(w: Workload, with_dO: bool = True):
-    return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_dO)
-
-
 def sample_indices(n_total: int, n_sample: int, seed: int = 1, must=()):
     """Seeded sample of distinct indices in [0, n_total), always holding `must`."""
     g = torch.Generator(device="cpu")
